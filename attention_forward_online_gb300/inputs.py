@@ -1,0 +1,112 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module only draws random tensors; it holds none of the attention
+arithmetic.  Both the CUDA path and the fp64 oracle are fed the same
+quantised bytes produced here.
+
+Recipe: a CPU ``torch.Generator`` seeded per workload draws, in this order,
+Q, K and V as ``torch.randn`` in fp32, each multiplied by its standard
+deviation, then rounded to the workload dtype (round-to-nearest-even).  The
+pages use no dataset; the five workloads below reproduce the shapes and value
+distributions the attention forward pass is specified on (the LLaMA-2-13B
+head shape H=40, d=128 at batch 8 / sequence 2048 is the one the
+"FlashAttention 2.0" article times on an A100).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Tuple
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str            # "bf16" or "fp32"
+    B: int
+    H: int
+    Nq: int
+    Nkv: int
+    d: int
+    causal: bool
+    key_len: Optional[Tuple[int, ...]]
+    seed: int
+    q_std: float = 1.0
+    kv_std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Nominal forward FLOPs: 4*B*H*Nq*Nkv*d, halved when causal."""
+        f = 4.0 * self.B * self.H * self.Nq * self.Nkv * self.d
+        return f / 2 if self.causal else f
+
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("fp32_b1_h1_n128_d64", "fp32", 1, 1, 128, 128, 64, False, None, seed=0),
+        Workload("bf16_b2_h4_n1024_d64_keypad", "bf16", 2, 4, 1024, 1024, 64, False,
+                 (1024, 724), seed=1),
+        Workload("bf16_causal_b4_h16_n4096_d64", "bf16", 4, 16, 4096, 4096, 64, True,
+                 None, seed=2),
+        Workload("bf16_b8_h40_n2048_d128", "bf16", 8, 40, 2048, 2048, 128, False, None,
+                 seed=3),
+        Workload("bf16_causal_b1_h32_n16384_d128_qstd3", "bf16", 1, 32, 16384, 16384, 128,
+                 True, None, seed=4, q_std=3.0),
+    ]
+}
+
+# The workload the benchmark times by default: the largest bf16 one.
+BENCH_WORKLOAD = "bf16_causal_b1_h32_n16384_d128_qstd3"
+
+
+def make_qkv(B: int, H: int, Nq: int, Nkv: int, d: int, dtype, seed: int,
+             q_std: float = 1.0, kv_std: float = 1.0):
+    """Q [B,H,Nq,d], K and V [B,H,Nkv,d] on the CPU, drawn as described above."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H, Nkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nkv, d), generator=g, dtype=torch.float32)
+    if q_std != 1.0:
+        q.mul_(q_std)
+    if kv_std != 1.0:
+        k.mul_(kv_std)
+        v.mul_(kv_std)
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def make_inputs(w: Workload):
+    """(Q, K, V, key_len or None) for a workload, on the CPU."""
+    q, k, v = make_qkv(w.B, w.H, w.Nq, w.Nkv, w.d, w.torch_dtype(), w.seed, w.q_std, w.kv_std)
+    kl = None if w.key_len is None else torch.tensor(w.key_len, dtype=torch.int32)
+    return q, k, v, kl
+
+
+def sample_rows(B: int, H: int, Nq: int, n: int, seed: int, include_edges: bool = True):
+    """A seeded list of flat row indices (b*H+h)*Nq+i for spot checks at full
+    size; always includes the first and last row of the first and last
+    (b, h) and the rows around every 128-row tile edge of one head."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    total = B * H * Nq
+    picks = set(torch.randint(0, total, (n,), generator=g).tolist())
+    if include_edges:
+        last_bh = (B * H - 1) * Nq
+        for base in (0, last_bh):
+            picks.update({base, base + Nq - 1})
+        bh = int(torch.randint(0, B * H, (1,), generator=g))
+        for t in range(0, Nq, 128):
+            for off in (t, t + 127):
+                if off < Nq:
+                    picks.add(bh * Nq + off)
+    return sorted(picks)

@@ -1,0 +1,335 @@
+// osattn_ref.cpp - fp64 CPU oracle for the attention forward pass.
+//
+// TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+// benchmark's CPU-baseline leg load this library.  The product (libosattn)
+// shares no code, header, table or helper with it, and it never calls into
+// the product.
+//
+// Sources (the three web pages on online softmax; cited by title + section):
+//   [Ch6]  "CUDA 算子工程：手写 FlashAttention v2 之路", chapter 6
+//          "Softmax 与 Online Softmax" (yangyitao.com).  This page decides
+//          what the method computes.
+//   [XXQK] m.xxqk.cn/news/563265, the article on why softmax parallelises
+//          and how FlashAttention uses online softmax (sections 1-7).
+//
+// What the oracle computes, for every query row i of every (b, h):
+//   J   = { j : j < clamp(key_len[b], 0, Nkv)  and  (not causal or j <= i) }
+//   s_j = scale * sum_k Q[i,k] K[j,k]                 ([XXQK] §1.1 steps 1-2,
+//                                                       scale then mask)
+//   J empty  ->  O[i,:] = 0, LSE = -inf               (fully masked row: the
+//                                                       library's contract;
+//                                                       [Ch6] §6.7.3 leaves
+//                                                       it undefined)
+//   else the three-pass safe softmax of [Ch6] §6.2:
+//     pass 1  m = max_j s_j
+//     pass 2  l = sum_j exp(s_j - m)
+//     pass 3  p_j = exp(s_j - m) / l,  O[i,:] = sum_j p_j V[j,:]
+//   LSE = m + log(l)                                   ([Ch6] §6.5)
+// in double precision throughout, on the exact values the GPU reads (bf16 /
+// fp32 inputs are widened to double without rounding).
+//
+// The scalar helpers below restate the other pieces of [Ch6] so that tests
+// can pin them independently: the unguarded two-pass definition (§6.1), the
+// one-element-at-a-time online recurrence (§6.3.1) with the -inf guard of
+// §6.4, the (m, l) combine (§6.4.1), and the blocked attention loop of §6.6
+// in both its forms (local max + beta, and the variant that exponentiates
+// against the new running max directly).  Parity of everything here is
+// pinned by tests/test_oracle.py (worked example, closed forms, library
+// routines, brute force); no function here is "parity unpinned".
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+const double kNegInf = -std::numeric_limits<double>::infinity();
+
+// Element formats the oracle can read.  bf16 is the top half of an IEEE
+// binary32, so widening is a shift; every bf16/fp32 value is exact in double.
+enum RefDtype { REF_BF16 = 0, REF_FP32 = 1, REF_FP64 = 2 };
+
+inline double load_elem(const void* base, int dtype, int64_t idx) {
+  if (dtype == REF_BF16) {
+    uint16_t h;
+    std::memcpy(&h, static_cast<const uint16_t*>(base) + idx, 2);
+    uint32_t u = static_cast<uint32_t>(h) << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return static_cast<double>(f);
+  }
+  if (dtype == REF_FP32) {
+    float f;
+    std::memcpy(&f, static_cast<const float*>(base) + idx, 4);
+    return static_cast<double>(f);
+  }
+  double v;
+  std::memcpy(&v, static_cast<const double*>(base) + idx, 8);
+  return v;
+}
+
+struct AttnProblem {
+  const void* Q;
+  const void* K;
+  const void* V;
+  int dtype;
+  int B, H, Nq, Nkv, d;
+  double scale;
+  int causal;
+  const int32_t* key_len;  // host array [B] or null
+};
+
+// Number of keys the batch entry may see: key_len clamped to [0, Nkv].
+int visible_keys(const AttnProblem& p, int b) {
+  if (!p.key_len) return p.Nkv;
+  int kl = p.key_len[b];
+  if (kl < 0) kl = 0;
+  if (kl > p.Nkv) kl = p.Nkv;
+  return kl;
+}
+
+// Computes one output row by the definition above.  `s` is scratch of Nkv
+// doubles.  flat_row = (b*H + h)*Nq + i.
+void attention_row(const AttnProblem& p, int64_t flat_row, double* o_row,
+                   double* lse, std::vector<double>& s) {
+  const int64_t bh = flat_row / p.Nq;
+  const int i = static_cast<int>(flat_row % p.Nq);
+  const int b = static_cast<int>(bh / p.H);
+  const int d = p.d;
+  int jend = visible_keys(p, b);
+  if (p.causal) jend = std::min(jend, i + 1);  // j <= i
+  for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+  if (jend <= 0) {  // J is empty
+    *lse = kNegInf;
+    return;
+  }
+  const int64_t qoff = flat_row * d;
+  const int64_t kvoff = bh * static_cast<int64_t>(p.Nkv) * d;
+  // logits s_j = scale * <q_i, k_j>
+  for (int j = 0; j < jend; ++j) {
+    double acc = 0.0;
+    const int64_t koff = kvoff + static_cast<int64_t>(j) * d;
+    for (int k = 0; k < d; ++k)
+      acc += load_elem(p.Q, p.dtype, qoff + k) * load_elem(p.K, p.dtype, koff + k);
+    s[j] = p.scale * acc;
+  }
+  // pass 1: row max
+  double m = kNegInf;
+  for (int j = 0; j < jend; ++j) m = std::max(m, s[j]);
+  // pass 2: denominator
+  double l = 0.0;
+  for (int j = 0; j < jend; ++j) l += std::exp(s[j] - m);
+  // pass 3: probabilities and the weighted sum of V rows
+  for (int j = 0; j < jend; ++j) {
+    const double pj = std::exp(s[j] - m) / l;
+    const int64_t voff = kvoff + static_cast<int64_t>(j) * d;
+    for (int c = 0; c < d; ++c) o_row[c] += pj * load_elem(p.V, p.dtype, voff + c);
+  }
+  *lse = m + std::log(l);
+}
+
+int check_problem(const AttnProblem& p) {
+  if (!p.Q || !p.K || !p.V) return 1;
+  if (p.B < 1 || p.H < 1 || p.Nq < 1 || p.Nkv < 1 || p.d < 1) return 1;
+  if (p.dtype < REF_BF16 || p.dtype > REF_FP64) return 1;
+  return 0;
+}
+
+template <class F>
+void parallel_rows(int64_t nrows, int nthreads, F&& body) {
+  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
+  if (nthreads <= 0) nthreads = 1;
+  if (nthreads > nrows) nthreads = static_cast<int>(std::max<int64_t>(nrows, 1));
+  std::atomic<int64_t> next(0);
+  const int64_t chunk = 16;
+  auto worker = [&]() {
+    for (;;) {
+      int64_t r0 = next.fetch_add(chunk);
+      if (r0 >= nrows) break;
+      int64_t r1 = std::min(nrows, r0 + chunk);
+      for (int64_t r = r0; r < r1; ++r) body(r);
+    }
+  };
+  std::vector<std::thread> pool;
+  for (int t = 1; t < nthreads; ++t) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+int osattn_ref_version(void) { return 1; }
+
+// [Ch6] §6.1: the direct two-pass definition e^{x_i} / sum_j e^{x_j}, with no
+// max subtraction (overflows for large inputs; used only on small ones).
+int osattn_ref_softmax_naive(const double* x, int n, double* y) {
+  if (!x || !y || n < 1) return 1;
+  double sum = 0.0;
+  for (int i = 0; i < n; ++i) sum += std::exp(x[i]);
+  for (int i = 0; i < n; ++i) y[i] = std::exp(x[i]) / sum;
+  return 0;
+}
+
+// [Ch6] §6.2: three-pass safe softmax.  Also returns m and l = sum e^{x-m}.
+// A row of only -inf has no defined softmax; it yields y = 0, m = -inf, l = 0.
+int osattn_ref_softmax_safe(const double* x, int n, double* y, double* m_out,
+                            double* l_out) {
+  if (!x || n < 1) return 1;
+  double m = kNegInf;
+  for (int i = 0; i < n; ++i) m = std::max(m, x[i]);
+  double l = 0.0;
+  if (m != kNegInf)
+    for (int i = 0; i < n; ++i) l += std::exp(x[i] - m);
+  if (y)
+    for (int i = 0; i < n; ++i) y[i] = (m == kNegInf) ? 0.0 : std::exp(x[i] - m) / l;
+  if (m_out) *m_out = m;
+  if (l_out) *l_out = l;
+  return 0;
+}
+
+// [Ch6] §6.3.1: the online recurrence from (m_0, l_0) = (-inf, 0),
+//   m_{n+1} = max(m_n, x_{n+1}),  l_{n+1} = l_n e^{m_n - m_{n+1}} + e^{x_{n+1} - m_{n+1}},
+// one element at a time, skipping the update while the running max is still
+// -inf (the guard of §6.4).  l_trace (optional) receives l_1 .. l_n.
+int osattn_ref_online_stats(const double* x, int n, double* m_out, double* l_out,
+                            double* l_trace) {
+  if (!x || n < 0 || !m_out || !l_out) return 1;
+  double m = kNegInf, l = 0.0;
+  for (int t = 0; t < n; ++t) {
+    const double m_new = std::max(m, x[t]);
+    if (m_new != kNegInf) {
+      l = l * std::exp(m - m_new) + std::exp(x[t] - m_new);
+      m = m_new;
+    }
+    if (l_trace) l_trace[t] = l;
+  }
+  *m_out = m;
+  *l_out = l;
+  return 0;
+}
+
+// [Ch6] §6.4.1: combine((m1,l1),(m2,l2)) = (M, l1 e^{m1-M} + l2 e^{m2-M}),
+// M = max(m1, m2); two empty states (-inf, 0) give the empty state back.
+void osattn_ref_combine(double m1, double l1, double m2, double l2, double* m_out,
+                        double* l_out) {
+  const double M = std::max(m1, m2);
+  if (M == kNegInf) {
+    *m_out = kNegInf;
+    *l_out = 0.0;
+    return;
+  }
+  *m_out = M;
+  *l_out = l1 * std::exp(m1 - M) + l2 * std::exp(m2 - M);
+}
+
+// [Ch6] §6.5: LSE = m + log l (natural log); -inf for the empty state.
+double osattn_ref_lse(double m, double l) {
+  if (m == kNegInf || l == 0.0) return kNegInf;
+  return m + std::log(l);
+}
+
+// Attention forward by the definition in the file header.
+//   Q: [B,H,Nq,d], K/V: [B,H,Nkv,d], contiguous, element format `dtype`
+//   (0 bf16 bits, 1 fp32, 2 fp64).  key_len: host int32 [B] or null.
+//   rows == null: every row; O receives [B,H,Nq,d], LSE [B,H,Nq].
+//   rows != null: only the nrows flat row indices (b*H+h)*Nq+i listed there;
+//   O receives [nrows,d] and LSE [nrows], in list order.
+//   nthreads <= 0 uses every hardware thread.
+// Returns 0, or 1 for an invalid argument (nothing written).
+int osattn_ref_attention_fwd(const void* Q, const void* K, const void* V, int dtype,
+                             double* O, double* LSE, int B, int H, int Nq, int Nkv,
+                             int d, double scale, int causal, const int32_t* key_len,
+                             const int64_t* rows, int64_t nrows, int nthreads) {
+  AttnProblem p{Q, K, V, dtype, B, H, Nq, Nkv, d, scale, causal, key_len};
+  if (check_problem(p) || !O || !LSE) return 1;
+  const int64_t total = static_cast<int64_t>(B) * H * Nq;
+  if (rows) {
+    if (nrows < 0) return 1;
+    for (int64_t r = 0; r < nrows; ++r)
+      if (rows[r] < 0 || rows[r] >= total) return 1;
+  } else {
+    nrows = total;
+  }
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    thread_local std::vector<double> s;
+    if (static_cast<int>(s.size()) < Nkv) s.resize(Nkv);
+    const int64_t flat = rows ? rows[r] : r;
+    attention_row(p, flat, O + r * d, LSE + r, s);
+  });
+  return 0;
+}
+
+// [Ch6] §6.6 / [XXQK] §4.1: the blocked ("FlashAttention") loop over key
+// blocks of `block` keys for every row, carrying (m, l, O).
+//   form 0: the §6.6 listing's form - a block-local max m_b, P = e^{S - m_b},
+//           l_b = rowsum P, then alpha = e^{m - m_new}, beta = e^{m_b - m_new},
+//           O = O alpha + beta P V_b, l = l alpha + beta l_b.
+//   form 1: the variant §6.6 notes as equivalent (and [XXQK] §4.1 prints):
+//           P = e^{S - m_new} directly, O = O alpha + P V_b, l = l alpha + rowsum P.
+// Masked keys (outside J) are skipped.  Blocks with no visible key leave the
+// state untouched (the -inf guard).  At the end O /= l and LSE = m + log l;
+// an empty J gives O = 0, LSE = -inf.  Same arguments/layout as
+// osattn_ref_attention_fwd (all rows).
+int osattn_ref_attention_blocked(const void* Q, const void* K, const void* V, int dtype,
+                                 double* O, double* LSE, int B, int H, int Nq, int Nkv,
+                                 int d, double scale, int causal, const int32_t* key_len,
+                                 int block, int form, int nthreads) {
+  AttnProblem p{Q, K, V, dtype, B, H, Nq, Nkv, d, scale, causal, key_len};
+  if (check_problem(p) || !O || !LSE || block < 1 || (form != 0 && form != 1)) return 1;
+  const int64_t total = static_cast<int64_t>(B) * H * Nq;
+  parallel_rows(total, nthreads, [&](int64_t flat) {
+    const int64_t bh = flat / Nq;
+    const int i = static_cast<int>(flat % Nq);
+    const int b = static_cast<int>(bh / H);
+    int jend = visible_keys(p, b);
+    if (causal) jend = std::min(jend, i + 1);
+    double* o = O + flat * d;
+    std::vector<double> sb(block), pv(d);
+    double m = kNegInf, l = 0.0;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int j0 = 0; j0 < jend; j0 += block) {
+      const int nb = std::min(block, jend - j0);
+      for (int t = 0; t < nb; ++t) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k)
+          acc += load_elem(Q, dtype, flat * d + k) *
+                 load_elem(K, dtype, (bh * Nkv + j0 + t) * d + k);
+        sb[t] = scale * acc;
+      }
+      double m_b = kNegInf;
+      for (int t = 0; t < nb; ++t) m_b = std::max(m_b, sb[t]);
+      const double m_new = std::max(m, m_b);
+      if (m_new == kNegInf) continue;
+      const double alpha = std::exp(m - m_new);
+      const double ref = (form == 0) ? m_b : m_new;
+      double l_b = 0.0;
+      for (int c = 0; c < d; ++c) pv[c] = 0.0;
+      for (int t = 0; t < nb; ++t) {
+        const double pt = std::exp(sb[t] - ref);
+        l_b += pt;
+        for (int c = 0; c < d; ++c) pv[c] += pt * load_elem(V, dtype, (bh * Nkv + j0 + t) * d + c);
+      }
+      const double beta = (form == 0) ? std::exp(m_b - m_new) : 1.0;
+      for (int c = 0; c < d; ++c) o[c] = o[c] * alpha + beta * pv[c];
+      l = l * alpha + beta * l_b;
+      m = m_new;
+    }
+    if (l > 0.0) {
+      for (int c = 0; c < d; ++c) o[c] /= l;
+      LSE[flat] = m + std::log(l);
+    } else {
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      LSE[flat] = kNegInf;
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"
