@@ -1,0 +1,205 @@
+// osattn_api.cu - the C ABI of libosattn (declared in include/osattn.h):
+// argument validation, per-device set-up, TMA descriptor encoding and kernel
+// selection.  Every step of the computation runs in the CUDA kernels; this
+// file only checks arguments and enqueues them.
+#include <cmath>
+#include <cstdint>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "osattn.h"
+#include "osattn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+// Device status: [0] = OSATTN_OK or OSATTN_ERR_TIMEOUT, [1] = site of the
+// first wait that gave up.  One copy per device that loads the library.
+__device__ unsigned int g_device_status[2];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
+std::atomic<int> g_last_timeout_site{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode_tiled = nullptr;
+
+// Per-device set-up, done once with the device current: SM count, the
+// device address of the status word, kernel attributes, and the driver's
+// tensor-map encoder.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return OSATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return OSATTN_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_device_status) !=
+        cudaSuccess)
+      return OSATTN_ERR_CUDA;
+    if (osattn::prepare_fwd_bf16() != cudaSuccess) return OSATTN_ERR_CUDA;
+    if (!g_encode_tiled) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return OSATTN_ERR_CUDA;
+      g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return OSATTN_OK;
+}
+
+// 3-D bf16 view (d, N, B*H) of a [B, H, N, d] tensor, 64 x 128 boxes,
+// 128-byte swizzle, zero fill outside the tensor.
+int encode_bf16_map(CUtensorMap* map, const void* base, int d, int N, long long BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {osattn::kBoxInner, osattn::kBoxRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+__global__ void wait_timeout_kernel(unsigned int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    osattn::mbar_init(&bar, 1);
+    abort_flag = 0;
+    osattn::fence_barrier_init();
+  }
+  __syncwarp();
+  // Nobody arrives on `bar`: the wait must give up after limit_ns.
+  const osattn::WaitCtl wc{&abort_flag, status, status + 1, limit_ns};
+  osattn::mbar_wait(&bar, 0, wc, 99u);
+}
+
+}  // namespace
+
+extern "C" {
+
+int osattn_version(void) { return OSATTN_VERSION; }
+
+const char* osattn_status_string(int status) {
+  switch (status) {
+    case OSATTN_OK: return "ok";
+    case OSATTN_ERR_INVALID_ARG: return "invalid argument";
+    case OSATTN_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
+    case OSATTN_ERR_CUDA: return "CUDA error";
+    case OSATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+               int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
+               int dtype, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return OSATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nkv < 1 || d < 1) return OSATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return OSATTN_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+      !aligned(LSE, 4) || (key_len && !aligned(key_len, 4)))
+    return OSATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return OSATTN_ERR_UNSUPPORTED;
+  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL) return OSATTN_ERR_INVALID_ARG;
+
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+
+  osattn::FwdArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.LSE = LSE;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nkv = Nkv;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.key_len = key_len;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = st->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = st->num_sms;
+
+  cudaError_t e;
+  if (dtype == OSATTN_FP32) {
+    e = osattn::launch_fwd_fp32(a);
+  } else {
+    CUtensorMap tmQ, tmK, tmV;
+    if (encode_bf16_map(&tmQ, Q, d, Nq, BH) != OSATTN_OK ||
+        encode_bf16_map(&tmK, K, d, Nkv, BH) != OSATTN_OK ||
+        encode_bf16_map(&tmV, V, d, Nkv, BH) != OSATTN_OK)
+      return OSATTN_ERR_CUDA;
+    e = osattn::launch_fwd_bf16(a, tmQ, tmK, tmV);
+  }
+  return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
+int osattn_get_device_status(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  unsigned int host[2] = {0, 0};
+  if (cudaMemcpy(host, st->status, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  const unsigned int zero[2] = {0, 0};
+  if (cudaMemcpy(st->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  if (host[0] != 0) g_last_timeout_site.store(static_cast<int>(host[1]));
+  return host[0] == 0 ? OSATTN_OK : static_cast<int>(host[0]);
+}
+
+int osattn_last_timeout_site(void) { return g_last_timeout_site.load(); }
+
+uint64_t osattn_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns < 1000 ? 1000 : ns);
+}
+
+int osattn_test_wait_timeout(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status,
+                                                                      g_wait_limit_ns.load());
+  return cudaGetLastError() == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
+}  // extern "C"

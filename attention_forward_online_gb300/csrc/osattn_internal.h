@@ -1,0 +1,41 @@
+// osattn_internal.h - launch interface between the C ABI (osattn_api.cu) and
+// the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace osattn {
+
+// Arguments of one forward call after host validation.
+struct FwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  float* LSE;
+  int B, H, Nq, Nkv, d;
+  float scale;
+  int causal;
+  const int32_t* key_len;  // device, may be null
+  cudaStream_t stream;
+  unsigned int* status;    // device status word [0] and give-up site [1]
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+
+// fp32 SIMT kernel (fwd_fp32_simt.cu).
+cudaError_t launch_fwd_fp32(const FwdArgs& a);
+
+// bf16 tcgen05 kernel (fwd_bf16_tcgen05.cu).  The tensor maps describe Q, K
+// and V as 3-D bf16 views (d, N, B*H) with 128-byte swizzled 64 x 128 boxes.
+cudaError_t prepare_fwd_bf16();  // once per device: kernel attributes
+cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV);
+
+// Box shape the bf16 kernel expects in its tensor maps.
+constexpr int kBoxInner = 64;   // elements along d (128 bytes)
+constexpr int kBoxRows = 128;   // rows of Q / K / V
+
+}  // namespace osattn

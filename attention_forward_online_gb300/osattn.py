@@ -1,0 +1,142 @@
+"""ctypes binding for libosattn (argument marshalling only).
+
+Every step of the forward pass runs in the library's CUDA kernels; this
+module checks tensor shapes, allocates outputs with torch (device memory is
+torch's job here), and passes raw pointers and the current stream through
+the C ABI declared in include/osattn.h.  If libosattn.so is missing the calls
+raise: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libosattn.so")
+
+BF16 = 0
+FP32 = 1
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 3
+ERR_TIMEOUT = 4
+
+EXPORTS = ("osattn_fwd", "osattn_status_string", "osattn_get_device_status",
+           "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
+           "osattn_last_timeout_site")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OsattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib():
+    """Load libosattn.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; "
+                    "g.build()\"` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32 = ctypes.c_void_p, ctypes.c_int
+            L.osattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     ctypes.c_float, i32, vp, i32, vp]
+            L.osattn_fwd.restype = i32
+            L.osattn_status_string.argtypes = [i32]
+            L.osattn_status_string.restype = ctypes.c_char_p
+            L.osattn_get_device_status.argtypes = [vp]
+            L.osattn_get_device_status.restype = i32
+            L.osattn_version.argtypes = []
+            L.osattn_version.restype = i32
+            L.osattn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.osattn_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.osattn_test_wait_timeout.argtypes = [vp]
+            L.osattn_test_wait_timeout.restype = i32
+            L.osattn_last_timeout_site.argtypes = []
+            L.osattn_last_timeout_site.restype = i32
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().osattn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nkv, d, scale, causal,
+            key_len_ptr, dtype, stream_handle) -> int:
+    """Direct call of osattn_fwd with integer pointers; returns the status."""
+    return lib().osattn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(Nq),
+                            int(Nkv), int(d), float(scale), int(bool(causal)), key_len_ptr,
+                            int(dtype), stream_handle)
+
+
+def fwd(q, k, v, scale: float | None = None, causal: bool = False, key_len=None,
+        out=None, lse=None, stream=None):
+    """O, LSE = attention forward of CUDA tensors q [B,H,Nq,d], k/v [B,H,Nkv,d].
+
+    dtype bf16 or fp32 (all three alike); key_len: None or a CUDA int32
+    tensor [B].  `out` / `lse` may be given preallocated (contiguous, the
+    right shape and dtype).  Enqueued on `stream` (default: torch's current
+    stream); raises OsattnError if the library rejects the call."""
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be bf16 or all fp32")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
+        raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    if tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be fp32 [B, H, Nq]")
+    kl_ptr = None
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise ValueError("key_len must be a CUDA int32 tensor with B entries")
+        key_len = key_len.contiguous()
+        kl_ptr = key_len.data_ptr()
+    dtype = BF16 if q.dtype == torch.bfloat16 else FP32
+    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                 B, H, Nq, Nkv, d, scale, causal, kl_ptr, dtype, _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_fwd")
+    return out, lse
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return lib().osattn_get_device_status(_stream_handle(stream))
+
+
+def version() -> int:
+    return lib().osattn_version()

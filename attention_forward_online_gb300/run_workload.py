@@ -1,0 +1,62 @@
+"""Run libosattn on one workload a fixed number of times (for profilers).
+
+    python -m attention_forward_online_gb300.run_workload --workload NAME
+        [--launches N] [--heads H]
+
+Inputs are the seeded synthetic tensors of the named workload, resident on
+cuda:0 before the first launch; --heads keeps only the first H heads (a
+smaller case of the same kernel for detailed Nsight Compute captures).
+Prints the mean launch time from CUDA events on the launching stream.
+"""
+import argparse
+import dataclasses
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None):
+    import torch
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import WORKLOADS, make_inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", required=True, choices=sorted(WORKLOADS))
+    ap.add_argument("--launches", type=int, default=4)
+    ap.add_argument("--heads", type=int, default=0)
+    args = ap.parse_args(argv)
+    w = WORKLOADS[args.workload]
+    if args.heads:
+        w = dataclasses.replace(w, H=min(args.heads, w.H))
+    q, k, v, kl = make_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    kld = None if kl is None else kl.to(dev)
+    O = torch.empty_like(qd)
+    L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.launches)]
+    with torch.cuda.stream(s):
+        for i in range(args.launches):
+            ev[2 * i].record(s)
+            osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O, lse=L,
+                       stream=s)
+            ev[2 * i + 1].record(s)
+    s.synchronize()
+    st = osattn.get_device_status(s)
+    if st != osattn.OK:
+        print("device status:", osattn.status_string(st))
+        return 1
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.launches)]
+    tf = [w.flops / (m * 1e-3) / 1e12 for m in ms]
+    print(f"{w.name} H={w.H}: launches {args.launches}, ms {['%.4f' % m for m in ms]}, "
+          f"TFLOPS {['%.1f' % t for t in tf]}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

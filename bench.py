@@ -1,0 +1,399 @@
+"""Benchmark of the attention forward pass (libosattn) on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one osattn_fwd call over the whole workload (every (b, h, query
+tile)).  The default workload is the largest bf16 one: causal B=1, H=32,
+N=16384, d=128, Q ~ N(0, 9), K, V ~ N(0, 1).  FLOPs per step are the nominal
+4*B*H*Nq*Nkv*d, halved for causal.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream with an L2 flush (a 256 MiB write) between steps
+outside the events; a barrier and a device synchronisation on both sides of
+the timed loop; the max over ranks.  nvidia-smi samples SM clocks and
+throttle reasons during the timed loop.  `e2e` repeats the measurement
+through the same C ABI call with the inputs in pinned host memory: every
+step copies Q, K, V host->device and O, LSE device->host inside the events.
+
+cpu_baseline: the fp64 oracle as it stands, timed on this host's cores on a
+bounded random sample of query rows of the same workload (about 10-20 s of
+CPU work) and scaled to TFLOPS by the sample's own FLOPs; the GPU's outputs
+on those rows give the max-abs error reported beside the throughput.
+
+--impl reference: times that oracle alone (rank 0; other ranks exit 0), each
+step a bounded row sample, and prints the same JSON line with
+"impl": "reference".
+
+N > 1 (torchrun): replicas only - every rank runs its own copy of the
+workload (no collective on the data path); value = total FLOPs of all ranks
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS on 1 GB300 and % of dense BF16 tensor peak; max-abs err vs oracle"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ("fwd_bf16_tcgen05.cu", "sm100_ptx.cuh")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "attention_forward_online_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the bf16 kernel from the committed ncu summary,
+    if it was taken on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=os.environ.get("OSATTN_DIST_BACKEND", "nccl"))
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (rank-local value if world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle leg
+def row_flops(w, rows):
+    """FLOPs the definition spends on the given flat rows: 4*d per visible key."""
+    total = 0
+    for r in rows:
+        i = r % w.Nq
+        vis = w.Nkv if not w.causal else min(w.Nkv, i + 1)
+        total += 4 * w.d * vis
+    return total
+
+
+def oracle_sample(w, q, k, v, n_rows, seed):
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    rows = sorted(set(rng.integers(0, w.B * w.H * w.Nq, size=n_rows).tolist()))
+    t0 = time.perf_counter()
+    O, L = oracle.attention_fwd(q, k, v, w.scale, w.causal, w.key_len, rows=rows)
+    dt = time.perf_counter() - t0
+    return rows, O, L, dt
+
+
+def calibrate_rows(w, q, k, v, target_s: float, seed: int):
+    """Number of sampled rows whose oracle time is about target_s."""
+    rows, _, _, dt = oracle_sample(w, q, k, v, 64, seed)
+    per_flop = dt / max(row_flops(w, rows), 1)
+    avg_row = row_flops(w, rows) / max(len(rows), 1)
+    return max(64, int(target_s / max(per_flop * avg_row, 1e-9)))
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    rank, _, world = int(os.environ.get("RANK", "0")), 0, int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    from attention_forward_online_gb300.inputs import make_inputs
+
+    q, k, v, _ = make_inputs(w)
+    n_rows = calibrate_rows(w, q, k, v, target_s=4.0, seed=1)
+    for s in range(args.warmup):
+        oracle_sample(w, q, k, v, n_rows, seed=100 + s)
+    flops, secs = 0, 0.0
+    for s in range(args.steps):
+        rows, _, _, dt = oracle_sample(w, q, k, v, n_rows, seed=1000 + s)
+        flops += row_flops(w, rows)
+        secs += dt
+    tflops = flops / secs / 1e12
+    sample = (f"{args.steps} steps x {n_rows} random query rows of {w.name} "
+              f"(of {w.B * w.H * w.Nq}), fp64, {secs:.1f} s total")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tflops, 6), "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "d": w.d,
+                   "causal": w.causal, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(tflops, 6), "unit": "TFLOPS", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(tflops, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w):
+    import torch
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import make_inputs
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    q, k, v, kl = make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    kld = None if kl is None else kl.to(dev)
+    O = torch.empty_like(qd)
+    L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O, lse=L,
+                   stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    if osattn.get_device_status(stream) != osattn.OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    # ---- device-resident timing
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # evict the previous step's lines from L2
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    barrier(world)
+    if osattn.get_device_status(stream) != osattn.OK:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    local_ms = sum(per_launch_ms)
+    total_ms = reduce_max(local_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_launch_ms = local_ms / args.steps
+    achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI from pinned host buffers
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    Lh = torch.empty(L.shape, dtype=L.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            flush.fill_(i & 0xFF)
+            es[i].record(stream)
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            step()
+            Oh.copy_(O, non_blocking=True)
+            Lh.copy_(L, non_blocking=True)
+            ee[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)), world) / e2e_steps
+    e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = Oh.numel() * Oh.element_size() + Lh.numel() * Lh.element_size()
+
+    line = None
+    if rank == 0:
+        # ---- oracle leg: CPU baseline on a bounded row sample + max-abs error
+        n_rows = calibrate_rows(w, q, k, v, target_s=args.cpu_seconds, seed=7)
+        rows, Oref, Lref, secs = oracle_sample(w, q, k, v, n_rows, seed=8)
+        cpu_tflops = row_flops(w, rows) / secs / 1e12
+        idx = torch.tensor(rows, device=dev)
+        Og = O.reshape(-1, w.d)[idx].double().cpu().numpy()
+        Lg = L.reshape(-1)[idx].double().cpu().numpy()
+        import numpy as np
+
+        fin = np.isfinite(Lref)
+        err_o = float(np.abs(Og - Oref).max())
+        err_l = float(np.abs(Lg[fin] - Lref[fin]).max()) if fin.any() else 0.0
+
+        peak = float(peaks["bf16_tflops"])
+        traffic = committed_traffic(w.name)
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv,
+                       "d": w.d, "causal": w.causal, "key_len": w.key_len,
+                       "flops_per_step": w.flops,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": round(100 * value / world / peak, 2),
+            "pct_of_bf16_peak_sustained": round(
+                100 * value / world / float(peaks["bf16_tflops_sustained"]), 2),
+            "max_abs_err": {"O": err_o, "LSE": err_l, "rows_checked": len(rows)},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3),
+                         "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "fwd_bf16_kernel" if w.dtype == "bf16" else "fwd_fp32_kernel",
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+            "cpu_baseline": {"value": round(cpu_tflops, 6), "unit": "TFLOPS",
+                             "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{len(rows)} random query rows of {w.name}, fp64, "
+                                       f"{secs:.1f} s"},
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOPS",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps,
+            "clocks": clock_info,
+            "kernel_source_sha": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    from attention_forward_online_gb300.inputs import BENCH_WORKLOAD, WORKLOADS
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

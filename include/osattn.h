@@ -1,0 +1,131 @@
+/*
+ * osattn.h - C ABI of libosattn, a fused scaled-dot-product attention forward
+ * pass for one NVIDIA GB300 (sm_103a), built on the one-pass online-softmax
+ * normaliser.
+ *
+ * Sources (cited by page title and section):
+ *   [Ch6]  "CUDA 算子工程：手写 FlashAttention v2 之路", chapter 6
+ *          "Softmax 与 Online Softmax" (yangyitao.com): the online (m, l)
+ *          recurrence (§6.3.1), the guarded combine (§6.4, §6.4.1), LSE
+ *          (§6.5), the blocked attention loop (§6.6), the fused additive
+ *          mask (§6.7.3).
+ *   [XXQK] m.xxqk.cn/news/563265 (article on parallel softmax and
+ *          FlashAttention): the attention problem statement (§1.1), the
+ *          inner loop with scale and mask and the single final O / l (§4.1),
+ *          the causal diagonal-block pitfall (§6.3).
+ *
+ * Every entry point is callable from C; no C++ or framework types cross it.
+ */
+#ifndef OSATTN_H
+#define OSATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSATTN_VERSION 1
+
+/* Element types of Q, K, V and O (LSE is always fp32). */
+#define OSATTN_BF16 0 /* bfloat16; runs on the tcgen05 tensor-core kernel */
+#define OSATTN_FP32 1 /* float32; runs on the SIMT kernel (full fp32 FMA) */
+
+/* Status codes. */
+#define OSATTN_OK 0
+#define OSATTN_ERR_INVALID_ARG 1 /* null pointer, size < 1, misalignment, non-finite scale */
+#define OSATTN_ERR_UNSUPPORTED 2 /* d or dtype outside the supported set */
+#define OSATTN_ERR_CUDA 3        /* a CUDA call failed (launch, attribute, tensor map) */
+#define OSATTN_ERR_TIMEOUT 4     /* a device-side wait ran past its limit (reported by
+                                    osattn_get_device_status only) */
+
+/*
+ * osattn_fwd - attention forward with online softmax.
+ *
+ * Computes, for every batch b < B, head h < H and query row i < Nq,
+ *     s_j    = scale * <Q[b,h,i,:], K[b,h,j,:]>                  ([XXQK] §1.1)
+ *     J      = { j < min(max(key_len[b], 0), Nkv) and (causal == 0 or j <= i) }
+ *     O[b,h,i,:] = sum_{j in J} e^{s_j} V[b,h,j,:] / sum_{j in J} e^{s_j}
+ *     LSE[b,h,i] = log sum_{j in J} e^{s_j}        (natural log, [Ch6] §6.5)
+ * by streaming K/V tiles with the running row max m and adjusted sum l
+ * ([Ch6] §6.3.1, §6.6), rescaling the accumulated O only when m changes and
+ * dividing by l once at the end ([XXQK] §4.1).  A row with J empty (keys all
+ * masked) gets O = 0 and LSE = -inf, never NaN.
+ *
+ * Arguments
+ *   Q        device, [B, H, Nq, d] contiguous, element type `dtype` (read)
+ *   K, V     device, [B, H, Nkv, d] contiguous, element type `dtype` (read)
+ *   O        device, [B, H, Nq, d] contiguous, element type `dtype` (written)
+ *   LSE      device, [B, H, Nq] contiguous fp32 (written)
+ *   B, H, Nq, Nkv   >= 1
+ *   d        head dimension: 64 or 128
+ *   scale    finite multiplier of the logits (1/sqrt(d) for the usual SDPA)
+ *   causal   0: no causal mask; non-zero: key j visible to query i iff j <= i
+ *            (top-left aligned, the same index for queries and keys)
+ *   key_len  device int32 [B] or NULL; keys j >= key_len[b] are masked
+ *            (values are clamped to [0, Nkv]; NULL means Nkv for every b).
+ *            Combined with `causal` by logical AND.
+ *   dtype    OSATTN_BF16 or OSATTN_FP32
+ *   stream   cudaStream_t to enqueue on (NULL: the legacy default stream)
+ *
+ * Layout and alignment: Q, K, V and O must be 16-byte aligned; LSE and
+ * key_len 4-byte aligned.  The d axis is fastest, then the sequence axis,
+ * then H, then B.  O and LSE must not overlap the inputs.
+ *
+ * Ownership: all buffers are owned by the caller and stay owned by it.  The
+ * call allocates no device memory and keeps no per-call state; it may read
+ * device properties and set kernel attributes once per device.
+ *
+ * Asynchrony and errors: the call validates its arguments on the host, then
+ * enqueues the kernel on `stream` and returns.  Results are valid once the
+ * stream has reached that point.  The return value covers host validation
+ * (OSATTN_ERR_INVALID_ARG / OSATTN_ERR_UNSUPPORTED, nothing enqueued) and
+ * launch failures (OSATTN_ERR_CUDA, read with cudaGetLastError, no
+ * synchronisation).  Device-side timeouts are reported by
+ * osattn_get_device_status.  Nothing is printed and nothing aborts.
+ */
+int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               int B, int H, int Nq, int Nkv, int d, float scale, int causal,
+               const int32_t* key_len, int dtype, void* stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char* osattn_status_string(int status);
+
+/*
+ * osattn_get_device_status - synchronises `stream`, then returns and clears
+ * the device status word of the current device: OSATTN_OK, or
+ * OSATTN_ERR_TIMEOUT if a kernel's bounded wait on an mbarrier ran past its
+ * limit since the last call (that kernel returned early; its outputs are
+ * undefined).  Returns OSATTN_ERR_CUDA if the synchronisation itself fails.
+ * Every device-side wait in libosattn is bounded; none traps.
+ */
+int osattn_get_device_status(void* stream);
+
+/* OSATTN_VERSION of the built library. */
+int osattn_version(void);
+
+/*
+ * Test hooks (no counterpart on the pages; they exist so the failure path can
+ * be exercised without faulting a GPU).
+ *
+ * osattn_set_wait_limit_ns - sets the time limit (nanoseconds, >= 1000) that
+ *   every device-side wait of later launches on any device uses; returns the
+ *   previous limit.  Default 4e9 (4 s).  Values below 1000 are clamped.
+ * osattn_test_wait_timeout - enqueues a one-warp kernel that waits on an
+ *   mbarrier nobody arrives on, with the current limit; the wait gives up,
+ *   records OSATTN_ERR_TIMEOUT in the status word and the kernel returns.
+ *   Returns OSATTN_OK or OSATTN_ERR_CUDA (launch failure).
+ */
+uint64_t osattn_set_wait_limit_ns(uint64_t ns);
+int osattn_test_wait_timeout(void* stream);
+
+/* Site code of the first wait that gave up, as read by the most recent
+ * osattn_get_device_status call that returned OSATTN_ERR_TIMEOUT (0 if none).
+ * Codes identify the waiting role (producer, MMA issuer, softmax, epilogue). */
+int osattn_last_timeout_site(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSATTN_H */

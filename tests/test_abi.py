@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/osattn.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run without a GPU; no call here reaches a kernel)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from attention_forward_online_gb300 import osattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from attention_forward_online_gb300 import _build
+
+    _build.build()
+    return osattn.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"^[A-Za-z_][\w \*]*?\b(osattn_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_every_declared_function_is_exported(L):
+    names = declared_functions()
+    assert {"osattn_fwd", "osattn_status_string", "osattn_get_device_status",
+            "osattn_version"} <= names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+    assert set(osattn.EXPORTS) == names
+
+
+def test_version_and_status_strings(L):
+    assert osattn.version() == 1
+    for code, text in [(0, "ok"), (1, "invalid argument"), (2, "unsupported"),
+                       (3, "CUDA error"), (4, "timed out"), (77, "unknown")]:
+        assert text in osattn.status_string(code)
+
+
+P = 0x10000  # a 16-byte aligned fake address; validation fails before it is used
+
+
+def call(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, Nq=8, Nkv=8, d=64, scale=0.125,
+             causal=0, key_len=None, dtype=osattn.BF16)
+    a.update(kw)
+    return osattn.fwd_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                          a["Nkv"], a["d"], a["scale"], a["causal"], a["key_len"], a["dtype"],
+                          ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), osattn.ERR_INVALID_ARG),
+    (dict(k=None), osattn.ERR_INVALID_ARG),
+    (dict(v=None), osattn.ERR_INVALID_ARG),
+    (dict(o=None), osattn.ERR_INVALID_ARG),
+    (dict(lse=None), osattn.ERR_INVALID_ARG),
+    (dict(B=0), osattn.ERR_INVALID_ARG),
+    (dict(H=-1), osattn.ERR_INVALID_ARG),
+    (dict(Nq=0), osattn.ERR_INVALID_ARG),
+    (dict(Nkv=0), osattn.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), osattn.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), osattn.ERR_INVALID_ARG),
+    (dict(q=P + 8), osattn.ERR_INVALID_ARG),
+    (dict(o=P + 2), osattn.ERR_INVALID_ARG),
+    (dict(lse=P + 2), osattn.ERR_INVALID_ARG),
+    (dict(key_len=P + 1), osattn.ERR_INVALID_ARG),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+    (dict(d=256), osattn.ERR_UNSUPPORTED),
+    (dict(dtype=7), osattn.ERR_UNSUPPORTED),
+])
+def test_host_validation_rejects_before_launch(L, kw, expect):
+    assert call(**kw) == expect
+
+
+def test_binding_rejects_cpu_tensors(L):
+    import torch
+
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        osattn.fwd(q, q, q)
+    with pytest.raises(TypeError):
+        osattn.fwd(q, q.float(), q)
