@@ -4,33 +4,40 @@
 //
 // The method is the blocked online-softmax loop of chapter 6 "Softmax 与
 // Online Softmax" of the hand-written FlashAttention v2 book (yangyitao.com):
-// a running row max m and adjusted sum l (§6.3.1), the guarded update when
+// a running row max m and adjusted sum l (§6.3.1), the guarded update while
 // every key so far is masked (§6.4), O rescaled by alpha = e^{m_old - m_new}
 // and P = e^{S - m_new} exponentiated against the new max (§6.6, the form
 // without beta), LSE = m + log l (§6.5); the scale and additive mask precede
 // the softmax and O / l happens once at the end (m.xxqk.cn/news/563265 §4.1).
-// Exponentials run in base 2 with scale * log2(e) folded into one multiply;
-// m and l live in those units and LSE converts back to natural log.
+// Exponentials run in base 2 with scale * log2(e) folded into one FMA; m and
+// l live in those units and LSE converts back to natural log.
 //
-// CTA layout (192 threads, one CTA per 128-row query tile of one (b, h)):
-//   warp 0        TMA producer: Q once, then K_0, K_1, V_0, K_2, V_1, ...
-//                 into a STAGES-deep ring of K/V tiles (one tile per stage),
-//                 in exactly the order the MMA warp consumes them.
-//   warp 1        allocates tensor memory; one thread issues the MMAs:
-//                 S_0, S_1, PV_0, S_2, PV_1, ... so S_{t+1} runs on the
-//                 tensor core while the softmax works on S_t.
-//   warps 2..5    softmax warpgroup, one query row per thread (tensor-memory
-//                 lane = row): reads S_t, masks, updates (m, l), writes
-//                 P_t = bf16(2^{x - m}) over S_t in tensor memory, rescales
-//                 O in tensor memory when some row's m moved, then the
-//                 epilogue O / l and LSE.
-// Tensor memory (512 columns): S double buffer at columns 0 and 128 (fp32,
-// 128 x 128 each; P_t overwrites the first 64 columns of its S buffer as
-// packed bf16 pairs), O at column 256 (fp32, 128 x d).
+// CTA layout: 512 threads own two 128-row query tiles (Q0, Q1) of one (b, h)
+// and stream that head's K/V tiles once for both.
+//   warps 0-3   softmax for tile 0, one query row per thread (tensor-memory
+//               lane = row); warps 4-7 the same for tile 1.  Per K/V tile:
+//               read S_t, mask if the tile crosses key_len or the diagonal,
+//               new row max, publish alpha, P_t = bf16(2^(x - m)) written
+//               over S_t in tensor memory, l = l * alpha + rowsum(P).
+//               At the end, the epilogue O / l and LSE for the tile.
+//   warps 8-11  correction: once PV_t of the previous K/V tile is done,
+//               multiply O_t by alpha in tensor memory - only warps holding
+//               a row whose max moved do it.  Off the softmax's path.
+//   warp 12     TMA producer: Q0, Q1 once, then K_0, V_0, K_1, V_1, ... into
+//               a STAGES-deep ring.
+//   warp 13     allocates tensor memory; one thread issues the MMAs in the
+//               order S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... so the
+//               tensor core computes one tile's S while the other tile's
+//               softmax runs (ping-pong between the two query tiles).
+// Tensor memory (512 columns): S0 at 0, S1 at 128 (fp32, 128 x 128 each; P_t
+// overwrites the first 64 columns of S_t as packed bf16 pairs), O0 at 256,
+// O1 at 256 + d (fp32, 128 x d).
+// Registers are rebalanced with setmaxnreg: softmax warps 184, correction 88,
+// producer / MMA warpgroup 56 (256x184 + 128x88 + 128x56 = 65536 = 512 threads
+// x 128 at launch; the host refuses a build with any other launch count).
 //
-// Tiles wholly outside the mask are never loaded or multiplied: the key loop
-// stops at min(key_len, last visible key of the tile's last row).  Only tiles
-// crossing key_len or the causal diagonal pay for element masking.
+// Tiles wholly outside the mask are never loaded or multiplied: each query
+// tile's key loop stops at min(key_len, last visible key of its last row).
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -41,11 +48,12 @@
 namespace osattn {
 namespace {
 
-constexpr int BM = 128;  // query rows per tile (MMA M, tensor-memory lanes)
-constexpr int BN = 128;  // keys per tile (MMA N of S = Q K^T, K of P V)
-constexpr int kThreads = 192;
+constexpr int BM = 128;     // query rows per tile (MMA M, tensor-memory lanes)
+constexpr int BN = 128;     // keys per K/V tile
+constexpr int kQTiles = 2;  // query tiles per CTA
+constexpr int kThreads = 512;
+constexpr int kCorrWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Give-up sites recorded in the status word's second slot.
@@ -55,29 +63,32 @@ enum : uint32_t {
   kSiteMmaKV = 3,
   kSiteMmaP = 4,
   kSiteSoftS = 5,
-  kSiteSoftO = 6,
-  kSiteEpiO = 7
+  kSiteCorrAlpha = 6,
+  kSiteCorrO = 7,
+  kSiteEpiO = 8
 };
 
 template <int HD>
 struct Cfg {
-  static constexpr int kColBlocks = HD / 64;           // 128-byte (64-element) column blocks
-  static constexpr int kTileBytes = BN * HD * 2;       // one K or V tile
-  static constexpr int kQBytes = BM * HD * 2;
-  static constexpr int kStages = HD == 128 ? 6 : 10;
-  static constexpr int kTileRegion = kQBytes + kStages * kTileBytes;
+  static constexpr int kTileBytes = BN * HD * 2;  // one K or V tile
+  static constexpr int kQBytes = BM * HD * 2;     // one query tile
+  static constexpr int kStages = HD == 128 ? 5 : 12;
+  static constexpr int kTileRegion = kQTiles * kQBytes + kStages * kTileBytes;
+  static constexpr uint32_t kOCol0 = 256;
 };
 
 struct __align__(8) Bars {
-  uint64_t q_full;
+  uint64_t q_full[kQTiles];
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full;
+  uint64_t s_full[kQTiles];      // MMA -> softmax: S_t ready
+  uint64_t alpha_full[kQTiles];  // softmax -> correction: alpha published (128 arrivals)
+  uint64_t p_full[kQTiles];      // softmax + correction -> MMA: P_t written, O_t rescaled (256)
+  uint64_t o_full[kQTiles];      // MMA -> correction / epilogue: PV_t done
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
+  float alpha[kQTiles][BM];
 };
 
 template <int HD>
@@ -90,15 +101,13 @@ struct Params {
   float* LSE;
   const int32_t* key_len;
   int H, Nq, Nkv;
-  int num_q_tiles;
+  int num_q_blocks;  // ceil(Nq / 256)
   float scale_log2;  // scale * log2(e)
   int causal;
   unsigned int* status;
   uint64_t wait_limit_ns;
 };
 
-// Waits on an mbarrier ignoring the abort flag (used only while draining
-// work that is already in flight), bounded by the wait limit.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_timer_ns();
@@ -107,10 +116,360 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-// Position of K_t / V_t in the producer's load sequence
-// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
-__device__ __forceinline__ int seq_of_k(int t) { return t == 0 ? 0 : 2 * t - 1; }
-__device__ __forceinline__ int seq_of_v(int t, int n) { return t == n - 1 ? 2 * n - 1 : 2 * t + 2; }
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Number of K/V tiles a query tile starting at row q0 must visit: keys
+// [0, min(key_len, q0 + BM if causal)); 0 when the tile lies beyond Nq or
+// sees no key.
+__device__ __forceinline__ int tile_kv_count(int q0, int Nq, int kv_len, int causal) {
+  if (q0 >= Nq) return 0;
+  int kv_end = kv_len;
+  if (causal) kv_end = min(kv_end, q0 + BM);
+  return (kv_end + BN - 1) / BN;
+}
+
+// Row max / min over 128 values: 3-input instructions in 8 chains.
+__device__ __forceinline__ float max128(const uint32_t* v) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(v[i]), __uint_as_float(v[i + 8]));
+#pragma unroll
+  for (int j = 16; j < BN; j += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      a[i] = fmax3(a[i], __uint_as_float(v[j + i]), __uint_as_float(v[j + 8 + i]));
+  return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
+__device__ __forceinline__ float min128(const uint32_t* v) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fminf(__uint_as_float(v[i]), __uint_as_float(v[i + 8]));
+#pragma unroll
+  for (int j = 16; j < BN; j += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      a[i] = fmin3(a[i], __uint_as_float(v[j + i]), __uint_as_float(v[j + 8 + i]));
+  return fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fminf(a[6], a[7]));
+}
+
+// ------------------------------------------------------------------ softmax
+// One thread per query row of tile t (tensor-memory lane = row).
+template <int HD>
+__device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32_t tmem, int t,
+                                             int bh, int q0, int n_t, int kv_len, WaitCtl wc) {
+  using C = Cfg<HD>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter+32)
+  const int row = quarter * 32 + lane;
+  const int qi = q0 + row;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint32_t s_addr = lane_base + static_cast<uint32_t>(t * BN);
+  const float c = p.scale_log2;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+
+  for (int j = 0; j < n_t; ++j) {
+    ok = mbar_wait(&bars->s_full[t], static_cast<uint32_t>(j) & 1u, wc, kSiteSoftS);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after_sync();
+    uint32_t v[BN];
+#pragma unroll
+    for (int ch = 0; ch < BN / 32; ++ch) tmem_ld_32x32b_x32(s_addr + ch * 32, v + ch * 32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int ch = 0; ch < BN / 32; ++ch) reg_fence32(v + ch * 32);
+
+    // x_j = s_j * c (log2 units).  Unmasked tiles keep raw s in v and fold
+    // the scale into the exponent's FMA (cm = c); tiles crossing key_len or
+    // the causal diagonal store x with -inf at masked keys (cm = 1).
+    const int k0 = j * BN;
+    float cm = c, m_new;
+    if (k0 + BN > kv_len || (p.causal && k0 + BN - 1 > q0)) {
+      const int lim = min(kv_len, p.causal ? qi + 1 : kv_len) - k0;  // visible: e < lim
+#pragma unroll
+      for (int e = 0; e < BN; ++e)
+        v[e] = __float_as_uint(e < lim ? __uint_as_float(v[e]) * c : -INFINITY);
+      cm = 1.f;
+      m_new = fmaxf(m, max128(v));
+    } else {
+      m_new = fmaxf(m, (c >= 0.f ? max128(v) : min128(v)) * c);
+    }
+    const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
+    bars->alpha[t][row] = alpha;
+    mbar_arrive(&bars->alpha_full[t]);
+
+    // P = 2^(x - m_new) in pairs (f32x2 FMA, two MUFU ex2, f32x2 add for the
+    // row sum), packed to bf16 and stored over S in two halves of 32
+    // columns.  A row with no visible key so far has m_new = -inf and x all
+    // -inf, so with neg_m = 0 every p is exactly 0 and (m, l) stays (-inf, 0).
+    const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+    const uint64_t cm2 = f2_pack(cm, cm), nm2 = f2_pack(neg_m, neg_m);
+    uint64_t rs_a = 0, rs_b = 0;  // packed partial row sums (bit pattern 0 = 0.0f)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = h * 64 + 2 * e;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), cm2, nm2),
+                  x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const uint64_t pp = f2_pack(p0, p1);
+        if (e & 1)
+          rs_b = f2_add(rs_b, pp);
+        else
+          rs_a = f2_add(rs_a, pp);
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_32x32b_x32(s_addr + h * 32, pk);
+    }
+    float r0, r1, r2, r3;
+    f2_unpack(rs_a, r0, r1);
+    f2_unpack(rs_b, r2, r3);
+    l = fmaf(l, alpha, (r0 + r1) + (r2 + r3));
+    m = m_new;
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(&bars->p_full[t]);
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  if (ok && n_t > 0) {
+    ok = mbar_wait(&bars->o_full[t], static_cast<uint32_t>(n_t - 1) & 1u, wc, kSiteEpiO);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) tc_fence_after_sync();
+  }
+  if (!ok) return;
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const uint64_t inv2 = f2_pack(inv_l, inv_l);
+  const bool store = qi < p.Nq;
+  __nv_bfloat16* orow = p.O + (static_cast<long long>(bh) * p.Nq + qi) * HD;
+  const uint32_t o_addr = lane_base + C::kOCol0 + static_cast<uint32_t>(t * HD);
+#pragma unroll
+  for (int ch = 0; ch < HD / 32; ++ch) {
+    uint32_t orr[32];
+    if (n_t > 0) {
+      tmem_ld_32x32b_x32(o_addr + ch * 32, orr);
+      tmem_ld_wait();
+      reg_fence32(orr);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) orr[e] = 0u;
+    }
+    uint32_t packed[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float a0, a1;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), inv2),
+                a0, a1);
+      packed[e] = pack_bf16x2(a0, a1);
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+    }
+  }
+  if (store)
+    p.LSE[static_cast<long long>(bh) * p.Nq + qi] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+// ------------------------------------------------------------------ correction
+// Multiplies O_t by alpha in tensor memory once PV_t of the previous K/V
+// tile has completed, for warps holding a row whose max moved; then signals
+// the MMA warp (together with the softmax) that PV_t may run.
+template <int HD>
+__device__ __forceinline__ void correction_tile(Bars* bars, uint32_t lane_base, int row, int t,
+                                                int j, bool& ok, WaitCtl wc) {
+  using C = Cfg<HD>;
+  ok = mbar_wait(&bars->alpha_full[t], static_cast<uint32_t>(j) & 1u, wc, kSiteCorrAlpha);
+  if (ok && j > 0)
+    ok = mbar_wait(&bars->o_full[t], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteCorrO);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return;
+  const float alpha = bars->alpha[t][row];
+  if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+    tc_fence_after_sync();
+    const uint64_t a2 = f2_pack(alpha, alpha);
+    const uint32_t o_addr = lane_base + C::kOCol0 + static_cast<uint32_t>(t * HD);
+#pragma unroll
+    for (int ch = 0; ch < HD / 32; ++ch) {
+      uint32_t orr[32];
+      tmem_ld_32x32b_x32(o_addr + ch * 32, orr);
+      tmem_ld_wait();
+      reg_fence32(orr);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float a0, a1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), a2),
+                  a0, a1);
+        orr[2 * e] = __float_as_uint(a0);
+        orr[2 * e + 1] = __float_as_uint(a1);
+      }
+      tmem_st_32x32b_x32(o_addr + ch * 32, orr);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before_sync();
+  mbar_arrive(&bars->p_full[t]);
+}
+
+template <int HD>
+__device__ __forceinline__ void correction_role(Bars* bars, uint32_t tmem, int n0, int n1,
+                                                WaitCtl wc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int n = max(n0, n1);
+  bool ok = true;
+  for (int j = 0; ok && j < n; ++j) {
+    if (j < n0) correction_tile<HD>(bars, lane_base, row, 0, j, ok, wc);
+    if (ok && j < n1) correction_tile<HD>(bars, lane_base, row, 1, j, ok, wc);
+  }
+}
+
+// ------------------------------------------------------------------ producer
+template <int HD>
+__device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, Bars* bars, uint8_t* sQ,
+                                              uint8_t* sKV, int bh, int q0, int n0, int n1,
+                                              WaitCtl wc) {
+  using C = Cfg<HD>;
+  if (n0 > 0) {
+    mbar_arrive_expect_tx(&bars->q_full[0], C::kQBytes);
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb)
+      tma_load_3d(sQ + cb * BM * 128, tmQ, &bars->q_full[0], cb * 64, q0, bh);
+  }
+  if (n1 > 0) {
+    mbar_arrive_expect_tx(&bars->q_full[1], C::kQBytes);
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb)
+      tma_load_3d(sQ + C::kQBytes + cb * BM * 128, tmQ, &bars->q_full[1], cb * 64, q0 + BM, bh);
+  }
+  const int total = 2 * max(n0, n1);  // K_0, V_0, K_1, V_1, ...
+  int u = 0;
+  for (; u < total; ++u) {
+    const int s = u % C::kStages;
+    const uint32_t round = static_cast<uint32_t>(u / C::kStages);
+    if (!mbar_wait(&bars->kv_empty[s], (round & 1u) ^ 1u, wc, kSiteProdEmpty)) break;
+    mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
+    uint8_t* dst = sKV + s * C::kTileBytes;
+    const CUtensorMap* map = (u & 1) ? tmV : tmK;
+#pragma unroll
+    for (int cb = 0; cb < HD / 64; ++cb)
+      tma_load_3d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (u >> 1) * BN, bh);
+  }
+  // Let every load this thread issued land before the CTA can exit.
+  if (n0 > 0) drain_wait(&bars->q_full[0], 0, wc.limit_ns);
+  if (n1 > 0) drain_wait(&bars->q_full[1], 0, wc.limit_ns);
+  for (int v = (u > C::kStages ? u - C::kStages : 0); v < u; ++v)
+    drain_wait(&bars->kv_full[v % C::kStages], static_cast<uint32_t>(v / C::kStages) & 1u,
+               wc.limit_ns);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// S_t = Q_t K^T: 128 x 128 fp32 into tensor-memory columns [t*128, t*128+128).
+// a_desc / b_desc address the first 16-element K slice; later slices move 32
+// bytes within a 128-byte swizzle row, or to the next 64-column block.
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);  // K-major A and B
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
+    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idS, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V: P from tensor memory (bf16 pairs over S_t), V MN-major in
+// shared memory; 16 keys per step = two 8-row swizzle atoms (2 KB).
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                         bool accumulate) {
+  constexpr uint32_t idPV = idesc_bf16_f32(BM, HD, 1);  // B (V) is MN-major
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_bf16_ts(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int HD>
+__device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ, uint8_t* sKV,
+                                         int n0, int n1, WaitCtl wc) {
+  using C = Cfg<HD>;
+  const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+  const uint64_t q_desc1 = q_desc0 + static_cast<uint64_t>(C::kQBytes >> 4);
+  const uint64_t k_desc = sdesc_sw128(smem_u32(sKV), 16, 1024);       // stage 0, K-major
+  const uint64_t v_desc = sdesc_sw128(smem_u32(sKV), BN * 128, 1024);  // stage 0, MN-major
+  constexpr uint64_t kStageStep = static_cast<uint64_t>(C::kTileBytes >> 4);
+  const uint32_t s_col0 = tmem, s_col1 = tmem + BN;
+  const uint32_t o_col0 = tmem + C::kOCol0, o_col1 = tmem + C::kOCol0 + HD;
+  const int n = max(n0, n1);
+  bool ok = true;
+
+  for (int j = 0; ok && j <= n; ++j) {
+    // K_j sits at load slot 2j, V_{j-1} at 2j - 1.
+    uint32_t vs = 0, ks = 0;
+    if (j > 0) {
+      const int u = 2 * j - 1;
+      vs = static_cast<uint32_t>(u % C::kStages);
+      ok = mbar_wait(&bars->kv_full[vs], static_cast<uint32_t>(u / C::kStages) & 1u, wc, kSiteMmaKV);
+    }
+    if (ok && j < n) {
+      const int u = 2 * j;
+      ks = static_cast<uint32_t>(u % C::kStages);
+      ok = mbar_wait(&bars->kv_full[ks], static_cast<uint32_t>(u / C::kStages) & 1u, wc, kSiteMmaKV);
+    }
+    if (ok && j == 0) {
+      if (n0 > 0) ok = mbar_wait(&bars->q_full[0], 0, wc, kSiteMmaQ);
+      if (ok && n1 > 0) ok = mbar_wait(&bars->q_full[1], 0, wc, kSiteMmaQ);
+    }
+    if (!ok) break;
+    tc_fence_after_sync();
+    // tile 0: PV0(j-1), then S0(j)
+    if (j > 0 && j - 1 < n0) {
+      ok = mbar_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_pv<HD>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
+      mma_commit(&bars->o_full[0]);
+    }
+    if (j < n0) {
+      issue_s<HD>(s_col0, q_desc0, k_desc + ks * kStageStep);
+      mma_commit(&bars->s_full[0]);
+    }
+    // tile 1: PV1(j-1), then S1(j)
+    if (j > 0 && j - 1 < n1) {
+      ok = mbar_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_pv<HD>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
+      mma_commit(&bars->o_full[1]);
+    }
+    if (j < n1) {
+      issue_s<HD>(s_col1, q_desc1, k_desc + ks * kStageStep);
+      mma_commit(&bars->s_full[1]);
+    }
+    if (j > 0) mma_commit(&bars->kv_empty[vs]);
+    if (j < n) mma_commit(&bars->kv_empty[ks]);
+  }
+  // Every MMA this thread issued must complete before tensor memory is freed.
+  mma_commit(&bars->mma_drain);
+  drain_wait(&bars->mma_drain, 0, wc.limit_ns);
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -121,44 +480,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = smem + C::kQBytes;
+  uint8_t* sKV = smem + kQTiles * C::kQBytes;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kTileRegion);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Work tile: all query tiles of one (b, h) are adjacent in launch order so
-  // CTAs running together share that head's K/V in L2; causal heads start
-  // with their longest query tiles.
-  const int bh = blockIdx.x / p.num_q_tiles;
-  int qt = blockIdx.x % p.num_q_tiles;
-  if (p.causal) qt = p.num_q_tiles - 1 - qt;
+  // Work unit: 256 query rows (two tiles) of one (b, h).  Units of a head
+  // are adjacent in launch order so concurrently running CTAs share that
+  // head's K/V in L2; causal heads start with their longest units.
+  const int bh = blockIdx.x / p.num_q_blocks;
+  int qb = blockIdx.x % p.num_q_blocks;
+  if (p.causal) qb = p.num_q_blocks - 1 - qb;
   const int b = bh / p.H;
   int kv_len = p.Nkv;
   if (p.key_len) kv_len = min(max(p.key_len[b], 0), p.Nkv);
-  const int q0 = qt * BM;
-  int kv_end = kv_len;
-  if (p.causal) kv_end = min(kv_end, q0 + BM);
-  const int n_tiles = (kv_end + BN - 1) / BN;
+  const int q0 = qb * (kQTiles * BM);
+  const int n0 = tile_kv_count(q0, p.Nq, kv_len, p.causal);
+  const int n1 = tile_kv_count(q0 + BM, p.Nq, kv_len, p.causal);
+  const int n = max(n0, n1);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->alpha_full[t], 128);
+      mbar_init(&bars->p_full[t], 256);
+      mbar_init(&bars->o_full[t], 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
-    }
-    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -168,249 +529,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, p.status, p.status + 1, p.wait_limit_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n_tiles > 0) {
-      mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
-#pragma unroll
-      for (int cb = 0; cb < C::kColBlocks; ++cb)
-        tma_load_3d(sQ + cb * BM * 128, &tmQ, &bars->q_full, cb * 64, q0, bh);
-      const int total = 2 * n_tiles;
-      int u = 0;
-      for (; u < total; ++u) {
-        // Decode which tile sequence slot u holds.
-        int kt;
-        bool is_v;
-        if (u == 0) {
-          kt = 0;
-          is_v = false;
-        } else if (u == total - 1) {
-          kt = n_tiles - 1;
-          is_v = true;
-        } else {
-          is_v = (u % 2) == 0;
-          kt = is_v ? (u - 2) / 2 : (u + 1) / 2;
-        }
-        const int s = u % C::kStages;
-        const uint32_t round = static_cast<uint32_t>(u / C::kStages);
-        if (!mbar_wait(&bars->kv_empty[s], (round & 1u) ^ 1u, wc, kSiteProdEmpty)) break;
-        mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
-        uint8_t* dst = sKV + s * C::kTileBytes;
-        const CUtensorMap* map = is_v ? &tmV : &tmK;
-#pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, kt * BN, bh);
-      }
-      // Let every load this thread issued land before the CTA can exit.
-      drain_wait(&bars->q_full, 0, p.wait_limit_ns);
-      for (int v = (u > C::kStages ? u - C::kStages : 0); v < u; ++v)
-        drain_wait(&bars->kv_full[v % C::kStages], static_cast<uint32_t>(v / C::kStages) & 1u,
-                   p.wait_limit_ns);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);   // K-major A and B
-      constexpr uint32_t idPV = idesc_bf16_f32(BM, HD, 1);  // B (V) is MN-major
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t kv_base = smem_u32(sKV);
-      bool ok = mbar_wait(&bars->q_full, 0, wc, kSiteMmaQ);
-      if (ok) tc_fence_after_sync();
-
-      auto issue_s = [&](int t) -> bool {
-        const int u = seq_of_k(t);
-        const int s = u % C::kStages;
-        if (!mbar_wait(&bars->kv_full[s], static_cast<uint32_t>(u / C::kStages) & 1u, wc,
-                       kSiteMmaKV))
-          return false;
-        tc_fence_after_sync();
-        const uint32_t d_col = tmem + ((t & 1) ? kSCol1 : kSCol0);
-        const uint32_t k_base = kv_base + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-          const uint64_t a = sdesc_sw128(q_base + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(k_base + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-          mma_bf16_ss(d_col, a, bdesc, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->kv_empty[s]);
-        mma_commit(&bars->s_full[t & 1]);
-        return true;
-      };
-      auto issue_pv = [&](int t) -> bool {
-        if (!mbar_wait(&bars->p_full[t & 1], static_cast<uint32_t>(t >> 1) & 1u, wc, kSiteMmaP))
-          return false;
-        const int u = seq_of_v(t, n_tiles);
-        const int s = u % C::kStages;
-        if (!mbar_wait(&bars->kv_full[s], static_cast<uint32_t>(u / C::kStages) & 1u, wc,
-                       kSiteMmaKV))
-          return false;
-        tc_fence_after_sync();
-        const uint32_t p_col = tmem + ((t & 1) ? kSCol1 : kSCol0);
-        const uint32_t v_base = kv_base + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // 16 keys per step = two 8-row swizzle atoms (2 KB); the d axis
-          // crosses 64-element column blocks BN * 128 bytes apart.
-          const uint64_t bdesc = sdesc_sw128(v_base + kk * 2048, BN * 128, 1024);
-          mma_bf16_ts(tmem + kOCol, p_col + kk * 8, bdesc, idPV, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars->kv_empty[s]);
-        mma_commit(&bars->o_full);
-        return true;
-      };
-
-      if (ok) ok = issue_s(0);
-      for (int t = 1; ok && t < n_tiles; ++t) {
-        ok = issue_s(t);
-        if (ok) ok = issue_pv(t - 1);
-      }
-      if (ok) issue_pv(n_tiles - 1);
-      // Every MMA this thread issued must complete before tensor memory is freed.
-      mma_commit(&bars->mma_drain);
-      drain_wait(&bars->mma_drain, 0, p.wait_limit_ns);
-    }
+  if (warp < kCorrWarp0) {
+    regs_inc<184>();
+    const int t = warp >> 2;
+    softmax_role<HD>(p, bars, tmem, t, bh, q0 + t * BM, t ? n1 : n0, kv_len, wc);
+  } else if (warp < kProducerWarp) {
+    regs_dec<88>();
+    correction_role<HD>(bars, tmem, n0, n1, wc);
   } else {
-    // ------------------------------------------------------------ softmax WG
-    const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter+32)
-    const int row = quarter * 32 + lane;
-    const int qi = q0 + row;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float c = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-
-    for (int t = 0; t < n_tiles; ++t) {
-      ok = mbar_wait(&bars->s_full[t & 1], static_cast<uint32_t>(t >> 1) & 1u, wc, kSiteSoftS);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const uint32_t s_addr = lane_base + ((t & 1) ? kSCol1 : kSCol0);
-      uint32_t sr[BN];
-#pragma unroll
-      for (int ch = 0; ch < BN / 32; ++ch) tmem_ld_32x32b_x32(s_addr + ch * 32, sr + ch * 32);
-      tmem_ld_wait();
-#pragma unroll
-      for (int ch = 0; ch < BN / 32; ++ch) reg_fence32(sr + ch * 32);
-
-      float x[BN];
-#pragma unroll
-      for (int j = 0; j < BN; ++j) x[j] = __uint_as_float(sr[j]) * c;
-      const int k0 = t * BN;
-      if (k0 + BN > kv_len || (p.causal && k0 + BN - 1 > q0)) {
-        // Tile crosses key_len or the causal diagonal: additive -inf mask.
-#pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          const int kj = k0 + j;
-          if (kj >= kv_len || (p.causal && kj > qi)) x[j] = -INFINITY;
-        }
-      }
-      float mx = x[0];
-#pragma unroll
-      for (int j = 1; j < BN; ++j) mx = fmaxf(mx, x[j]);
-      const float m_new = fmaxf(m, mx);
-      const bool changed = (m_new != m);
-      float alpha = 1.f;
-      uint32_t pk[BN / 2];
-      float rs = 0.f;
-      if (m_new == -INFINITY) {
-        // Every key so far is masked: the state stays (-inf, 0) and P = 0.
-#pragma unroll
-        for (int j = 0; j < BN / 2; ++j) pk[j] = 0u;
-      } else {
-        if (changed) alpha = ex2_approx(m - m_new);
-#pragma unroll
-        for (int j = 0; j < BN / 2; ++j) {
-          const float p0 = ex2_approx(x[2 * j] - m_new);
-          const float p1 = ex2_approx(x[2 * j + 1] - m_new);
-          rs += p0 + p1;
-          pk[j] = pack_bf16x2(p0, p1);
-        }
-      }
-      l = l * alpha + rs;
-      m = m_new;
-      tmem_st_32x32b_x32(s_addr, pk);
-      tmem_st_32x32b_x32(s_addr + 32, pk + 32);
-
-      if (t > 0) {
-        // O holds the sum through PV_{t-1}; rescale it by alpha once that
-        // MMA has finished, and only if some row of this warp moved its max.
-        bool okw = mbar_wait(&bars->o_full, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteSoftO);
-        okw = __all_sync(0xffffffffu, okw);
-        if (!okw) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, changed)) {
-#pragma unroll
-          for (int ch = 0; ch < HD / 32; ++ch) {
-            uint32_t orr[32];
-            const uint32_t o_addr = lane_base + kOCol + ch * 32;
-            tmem_ld_32x32b_x32(o_addr, orr);
-            tmem_ld_wait();
-            reg_fence32(orr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st_32x32b_x32(o_addr, orr);
-          }
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bars->p_full[t & 1]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait(&bars->o_full, static_cast<uint32_t>(n_tiles - 1) & 1u, wc, kSiteEpiO);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) tc_fence_after_sync();
-    }
-    if (ok) {
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool store = qi < p.Nq;
-      __nv_bfloat16* orow = p.O + (static_cast<long long>(bh) * p.Nq + qi) * HD;
-#pragma unroll
-      for (int ch = 0; ch < HD / 32; ++ch) {
-        uint32_t orr[32];
-        if (n_tiles > 0) {
-          tmem_ld_32x32b_x32(lane_base + kOCol + ch * 32, orr);
-          tmem_ld_wait();
-          reg_fence32(orr);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = 0u;
-        }
-        uint32_t packed[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          packed[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                                  __uint_as_float(orr[2 * e + 1]) * inv_l);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-        }
-      }
-      if (store)
-        p.LSE[static_cast<long long>(bh) * p.Nq + qi] =
-            l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-    }
+    regs_dec<56>();
+    if (warp == kProducerWarp && lane == 0 && n > 0)
+      producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, bh, q0, n0, n1, wc);
+    else if (warp == kMmaWarp && lane == 0 && n > 0)
+      mma_role<HD>(bars, tmem, sQ, sKV, n0, n1, wc);
   }
 
+  __syncwarp();
+  tmem_st_wait();
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
+// The setmaxnreg split above hands out exactly 512 x 128 registers; a build
+// whose launch register count differs would make setmaxnreg.inc wait
+// forever, so such a build is refused here instead of launched.
+constexpr int kLaunchRegs = 128;
+
 template <int HD>
 cudaError_t set_attrs() {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<HD>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   return cudaFuncSetAttribute(fwd_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes<HD>());
 }
@@ -432,12 +587,12 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
   p.H = a.H;
   p.Nq = a.Nq;
   p.Nkv = a.Nkv;
-  p.num_q_tiles = (a.Nq + BM - 1) / BM;
+  p.num_q_blocks = (a.Nq + kQTiles * BM - 1) / (kQTiles * BM);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.causal = a.causal;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
-  const long long grid = static_cast<long long>(p.num_q_tiles) * a.B * a.H;
+  const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
   if (a.d == 64)
