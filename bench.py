@@ -189,11 +189,18 @@ def oracle_sample(w, q, k, v, n_rows, seed):
 
 
 def calibrate_rows(w, q, k, v, target_s: float, seed: int):
-    """Number of sampled rows whose oracle time is about target_s."""
-    rows, _, _, dt = oracle_sample(w, q, k, v, 64, seed)
-    per_flop = dt / max(row_flops(w, rows), 1)
-    avg_row = row_flops(w, rows) / max(len(rows), 1)
-    return max(64, int(target_s / max(per_flop * avg_row, 1e-9)))
+    """Number of sampled rows whose oracle time is about target_s: one small
+    warm-up call (thread start-up, page faults), then a timed call whose row
+    count grows until it takes at least a quarter of a second."""
+    oracle_sample(w, q, k, v, 32, seed)
+    n = 256
+    while True:
+        rows, _, _, dt = oracle_sample(w, q, k, v, n, seed + 1)
+        if dt >= 0.25 or n >= 1 << 20:
+            break
+        n *= 4
+    per_row = dt / max(len(rows), 1)
+    return max(64, int(target_s / max(per_row, 1e-9)))
 
 
 def cpu_cores() -> int:
