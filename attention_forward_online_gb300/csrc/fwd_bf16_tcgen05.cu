@@ -99,8 +99,11 @@ constexpr int smem_bytes() {
 struct Params {
   __nv_bfloat16* O;
   float* LSE;
+  float* o_part;    // split-KV only: [splits, B*H, Nq, d] fp32 partial O (already / l_s)
+  float* lse_part;  // split-KV only: [splits, B*H, Nq] fp32 partial LSE
   const int32_t* key_len;
-  int H, Nq, Nkv;
+  int H, Nq, Nkv, BH;
+  int num_splits;
   int num_q_blocks;  // ceil(Nq / 256)
   float scale_log2;  // scale * log2(e)
   int causal;
@@ -162,9 +165,10 @@ __device__ __forceinline__ float min128(const uint32_t* v) {
 
 // ------------------------------------------------------------------ softmax
 // One thread per query row of tile t (tensor-memory lane = row).
-template <int HD>
+template <int HD, bool kSplit>
 __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32_t tmem, int t,
-                                             int bh, int q0, int n_t, int kv_len, WaitCtl wc) {
+                                             int bh, int q0, int n_t, int kv_len, int sb,
+                                             int split, WaitCtl wc) {
   using C = Cfg<HD>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter+32)
@@ -191,7 +195,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     // x_j = s_j * c (log2 units).  Unmasked tiles keep raw s in v and fold
     // the scale into the exponent's FMA (cm = c); tiles crossing key_len or
     // the causal diagonal store x with -inf at masked keys (cm = 1).
-    const int k0 = j * BN;
+    const int k0 = (sb + j) * BN;
     float cm = c, m_new;
     if (k0 + BN > kv_len || (p.causal && k0 + BN - 1 > q0)) {
       const int lim = min(kv_len, p.causal ? qi + 1 : kv_len) - k0;  // visible: e < lim
@@ -251,6 +255,37 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
   }
   if (!ok) return;
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const uint32_t o_addr_t = lane_base + C::kOCol0 + static_cast<uint32_t>(t * HD);
+  if constexpr (kSplit) {
+    // Partial result of this key range: O_s = O / l_s in fp32 and
+    // lse_s = m + ln l_s (or 0 and -inf for a range with no visible key),
+    // merged later by the combine kernel.  The tensor-memory loads are
+    // warp-wide; only the stores depend on the row.
+    const bool store = qi < p.Nq;
+    const long long prow = (static_cast<long long>(split) * p.BH + bh) * p.Nq + qi;
+    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * HD);
+#pragma unroll
+    for (int ch = 0; ch < HD / 32; ++ch) {
+      uint32_t orr[32];
+      if (n_t > 0) {
+        tmem_ld_32x32b_x32(o_addr_t + ch * 32, orr);
+        tmem_ld_wait();
+        reg_fence32(orr);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) orr[e] = 0u;
+      }
+      if (store) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dst[ch * 8 + e] = make_float4(
+              __uint_as_float(orr[4 * e]) * inv_l, __uint_as_float(orr[4 * e + 1]) * inv_l,
+              __uint_as_float(orr[4 * e + 2]) * inv_l, __uint_as_float(orr[4 * e + 3]) * inv_l);
+      }
+    }
+    if (store) p.lse_part[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    return;
+  }
   const uint64_t inv2 = f2_pack(inv_l, inv_l);
   const bool store = qi < p.Nq;
   __nv_bfloat16* orow = p.O + (static_cast<long long>(bh) * p.Nq + qi) * HD;
@@ -345,7 +380,7 @@ template <int HD>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, Bars* bars, uint8_t* sQ,
                                               uint8_t* sKV, int bh, int q0, int n0, int n1,
-                                              WaitCtl wc) {
+                                              int sb, WaitCtl wc) {
   using C = Cfg<HD>;
   if (n0 > 0) {
     mbar_arrive_expect_tx(&bars->q_full[0], C::kQBytes);
@@ -370,7 +405,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
     const CUtensorMap* map = (u & 1) ? tmV : tmK;
 #pragma unroll
     for (int cb = 0; cb < HD / 64; ++cb)
-      tma_load_3d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (u >> 1) * BN, bh);
+      tma_load_3d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (sb + (u >> 1)) * BN, bh);
   }
   // Let every load this thread issued land before the CTA can exit.
   if (n0 > 0) drain_wait(&bars->q_full[0], 0, wc.limit_ns);
@@ -471,7 +506,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
   drain_wait(&bars->mma_drain, 0, wc.limit_ns);
 }
 
-template <int HD>
+template <int HD, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -487,15 +522,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Work unit: 256 query rows (two tiles) of one (b, h).  Units of a head
   // are adjacent in launch order so concurrently running CTAs share that
   // head's K/V in L2; causal heads start with their longest units.
-  const int bh = blockIdx.x / p.num_q_blocks;
-  int qb = blockIdx.x % p.num_q_blocks;
+  int unit = blockIdx.x, split = 0;
+  if constexpr (kSplit) {  // key-range split fastest: splits of one unit run together
+    split = unit % p.num_splits;
+    unit /= p.num_splits;
+  }
+  const int bh = unit / p.num_q_blocks;
+  int qb = unit % p.num_q_blocks;
   if (p.causal) qb = p.num_q_blocks - 1 - qb;
   const int b = bh / p.H;
   int kv_len = p.Nkv;
   if (p.key_len) kv_len = min(max(p.key_len[b], 0), p.Nkv);
   const int q0 = qb * (kQTiles * BM);
-  const int n0 = tile_kv_count(q0, p.Nq, kv_len, p.causal);
-  const int n1 = tile_kv_count(q0 + BM, p.Nq, kv_len, p.causal);
+  int n0 = tile_kv_count(q0, p.Nq, kv_len, p.causal);
+  int n1 = tile_kv_count(q0 + BM, p.Nq, kv_len, p.causal);
+  int sb = 0;  // first K/V tile of this CTA's key range
+  if constexpr (kSplit) {
+    // The unit's K/V tiles [0, max(n0, n1)) are cut into num_splits equal
+    // ranges; each query tile visits the part of its own range inside ours.
+    const int n_all = max(n0, n1);
+    const int per = (n_all + p.num_splits - 1) / p.num_splits;
+    sb = min(n_all, split * per);
+    const int se = min(n_all, sb + per);
+    n0 = max(0, min(se, n0) - sb);
+    n1 = max(0, min(se, n1) - sb);
+  }
   const int n = max(n0, n1);
 
   if (threadIdx.x == 0) {
@@ -532,14 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kCorrWarp0) {
     regs_inc<184>();
     const int t = warp >> 2;
-    softmax_role<HD>(p, bars, tmem, t, bh, q0 + t * BM, t ? n1 : n0, kv_len, wc);
+    softmax_role<HD, kSplit>(p, bars, tmem, t, bh, q0 + t * BM, t ? n1 : n0, kv_len, sb, split, wc);
   } else if (warp < kProducerWarp) {
     regs_dec<88>();
     correction_role<HD>(bars, tmem, n0, n1, wc);
   } else {
     regs_dec<56>();
     if (warp == kProducerWarp && lane == 0 && n > 0)
-      producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, bh, q0, n0, n1, wc);
+      producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, bh, q0, n0, n1, sb, wc);
     else if (warp == kMmaWarp && lane == 0 && n > 0)
       mma_role<HD>(bars, tmem, sQ, sKV, n0, n1, wc);
   }
@@ -560,22 +611,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // forever, so such a build is refused here instead of launched.
 constexpr int kLaunchRegs = 128;
 
-template <int HD>
+template <int HD, bool kSplit>
 cudaError_t set_attrs() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<HD>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<HD, kSplit>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(fwd_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              smem_bytes<HD>());
+  return cudaFuncSetAttribute(fwd_bf16_kernel<HD, kSplit>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<HD>());
 }
 
 }  // namespace
 
 cudaError_t prepare_fwd_bf16() {
-  cudaError_t e = set_attrs<64>();
-  if (e != cudaSuccess) return e;
-  return set_attrs<128>();
+  cudaError_t e;
+  if ((e = set_attrs<64, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<128, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<64, true>()) != cudaSuccess) return e;
+  return set_attrs<128, true>();
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -583,22 +636,34 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
   Params p;
   p.O = static_cast<__nv_bfloat16*>(a.O);
   p.LSE = a.LSE;
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
   p.key_len = a.key_len;
   p.H = a.H;
   p.Nq = a.Nq;
   p.Nkv = a.Nkv;
+  p.BH = a.B * a.H;
+  p.num_splits = a.num_splits > 0 ? a.num_splits : 1;
   p.num_q_blocks = (a.Nq + kQTiles * BM - 1) / (kQTiles * BM);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.causal = a.causal;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
-  const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H;
+  const bool split = a.num_splits > 0;
+  const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H * p.num_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
-  if (a.d == 64)
-    fwd_bf16_kernel<64><<<g, blk, smem_bytes<64>(), a.stream>>>(tmQ, tmK, tmV, p);
-  else
-    fwd_bf16_kernel<128><<<g, blk, smem_bytes<128>(), a.stream>>>(tmQ, tmK, tmV, p);
+  if (a.d == 64) {
+    if (split)
+      fwd_bf16_kernel<64, true><<<g, blk, smem_bytes<64>(), a.stream>>>(tmQ, tmK, tmV, p);
+    else
+      fwd_bf16_kernel<64, false><<<g, blk, smem_bytes<64>(), a.stream>>>(tmQ, tmK, tmV, p);
+  } else {
+    if (split)
+      fwd_bf16_kernel<128, true><<<g, blk, smem_bytes<128>(), a.stream>>>(tmQ, tmK, tmV, p);
+    else
+      fwd_bf16_kernel<128, false><<<g, blk, smem_bytes<128>(), a.stream>>>(tmQ, tmK, tmV, p);
+  }
   return cudaGetLastError();
 }
 

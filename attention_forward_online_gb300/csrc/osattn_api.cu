@@ -120,9 +120,15 @@ const char* osattn_status_string(int status) {
   }
 }
 
-int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-               int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
-               int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host validation shared by every forward entry point; nothing is enqueued
+// when it fails.
+int validate_fwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                 int B, int H, int Nq, int Nkv, int d, float scale, const int32_t* key_len,
+                 int dtype) {
   if (!Q || !K || !V || !O || !LSE) return OSATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Nq < 1 || Nkv < 1 || d < 1) return OSATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return OSATTN_ERR_INVALID_ARG;
@@ -131,13 +137,13 @@ int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
     return OSATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return OSATTN_ERR_UNSUPPORTED;
   if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
-  const long long BH = static_cast<long long>(B) * H;
-  if (BH > 0x7fffffffLL) return OSATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return OSATTN_ERR_INVALID_ARG;
+  return OSATTN_OK;
+}
 
-  DeviceState* st = nullptr;
-  int rc = device_state(&st);
-  if (rc != OSATTN_OK) return rc;
-
+osattn::FwdArgs make_args(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                          int H, int Nq, int Nkv, int d, float scale, int causal,
+                          const int32_t* key_len, void* stream, const DeviceState* st) {
   osattn::FwdArgs a;
   a.Q = Q;
   a.K = K;
@@ -156,19 +162,85 @@ int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
   a.status = st->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.num_sms = st->num_sms;
+  return a;
+}
 
+int encode_qkv(const void* Q, const void* K, const void* V, int d, int Nq, int Nkv, long long BH,
+               CUtensorMap* tmQ, CUtensorMap* tmK, CUtensorMap* tmV) {
+  if (encode_bf16_map(tmQ, Q, d, Nq, BH) != OSATTN_OK ||
+      encode_bf16_map(tmK, K, d, Nkv, BH) != OSATTN_OK ||
+      encode_bf16_map(tmV, V, d, Nkv, BH) != OSATTN_OK)
+    return OSATTN_ERR_CUDA;
+  return OSATTN_OK;
+}
+
+// Split-KV launch over caller-provided partial buffers: the key-range split
+// of the bf16 kernel, then the combine.  Arguments are already validated.
+int launch_splitkv(osattn::FwdArgs a, int num_splits, float* o_part, float* lse_part) {
+  CUtensorMap tmQ, tmK, tmV;
+  const long long BH = static_cast<long long>(a.B) * a.H;
+  if (encode_qkv(a.Q, a.K, a.V, a.d, a.Nq, a.Nkv, BH, &tmQ, &tmK, &tmV) != OSATTN_OK)
+    return OSATTN_ERR_CUDA;
+  a.num_splits = num_splits;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  if (osattn::launch_fwd_bf16(a, tmQ, tmK, tmV) != cudaSuccess) return OSATTN_ERR_CUDA;
+  if (osattn::launch_splitkv_combine(o_part, lse_part, a.O, a.LSE, BH * a.Nq, a.d, num_splits,
+                                     a.stream) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  return OSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+               int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
+               int dtype, void* stream) {
+  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  osattn::FwdArgs a = make_args(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, causal, key_len, stream, st);
   cudaError_t e;
   if (dtype == OSATTN_FP32) {
     e = osattn::launch_fwd_fp32(a);
   } else {
     CUtensorMap tmQ, tmK, tmV;
-    if (encode_bf16_map(&tmQ, Q, d, Nq, BH) != OSATTN_OK ||
-        encode_bf16_map(&tmK, K, d, Nkv, BH) != OSATTN_OK ||
-        encode_bf16_map(&tmV, V, d, Nkv, BH) != OSATTN_OK)
+    if (encode_qkv(Q, K, V, d, Nq, Nkv, static_cast<long long>(B) * H, &tmQ, &tmK, &tmV) !=
+        OSATTN_OK)
       return OSATTN_ERR_CUDA;
     e = osattn::launch_fwd_bf16(a, tmQ, tmK, tmV);
   }
   return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
+size_t osattn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                       int H, int Nq, int Nkv, int d, float scale, int causal,
+                       const int32_t* key_len, int dtype, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (dtype != OSATTN_BF16) return OSATTN_ERR_UNSUPPORTED;
+  if (num_splits < 1 || num_splits > OSATTN_MAX_SPLITS) return OSATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  osattn::FwdArgs a = make_args(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, causal, key_len, stream, st);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = o_part + static_cast<size_t>(num_splits) * B * H * Nq * d;
+  return launch_splitkv(a, num_splits, o_part, lse_part);
 }
 
 int osattn_get_device_status(void* stream) {

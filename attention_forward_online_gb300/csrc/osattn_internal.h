@@ -23,6 +23,11 @@ struct FwdArgs {
   unsigned int* status;    // device status word [0] and give-up site [1]
   uint64_t wait_limit_ns;
   int num_sms;
+  // split-KV only (num_splits > 0): fp32 partials [num_splits, B*H, Nq, d]
+  // and their LSE [num_splits, B*H, Nq]
+  int num_splits = 0;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
 };
 
 // fp32 SIMT kernel (fwd_fp32_simt.cu).
@@ -33,6 +38,12 @@ cudaError_t launch_fwd_fp32(const FwdArgs& a);
 cudaError_t prepare_fwd_bf16();  // once per device: kernel attributes
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV);
+
+// Split-KV combine (splitkv_combine.cu): folds the partials of each row with
+// the (m, l) combine and writes O (bf16) and LSE.
+cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* O,
+                                   float* LSE, long long rows, int d, int num_splits,
+                                   cudaStream_t stream);
 
 // Box shape the bf16 kernel expects in its tensor maps.
 constexpr int kBoxInner = 64;   // elements along d (128 bytes)

@@ -35,6 +35,7 @@ class Workload:
     seed: int
     q_std: float = 1.0
     kv_std: float = 1.0
+    splits: int = 0  # > 0: measured through the split-KV entry point with this many ranges
 
     @property
     def scale(self) -> float:
@@ -62,6 +63,17 @@ WORKLOADS = {
                  seed=3),
         Workload("bf16_causal_b1_h32_n16384_d128_qstd3", "bf16", 1, 32, 16384, 16384, 128,
                  True, None, seed=4, q_std=3.0),
+    ]
+}
+
+# Workloads for the split-KV path: few (b, h) rows with long key sequences,
+# where one CTA per 256 query rows cannot fill 152 SMs (16 CTAs here); the
+# key axis is cut into 9 ranges (144 CTAs).
+SPLITKV_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("bf16_b1_h8_q512_kv65536_d128", "bf16", 1, 8, 512, 65536, 128, False, None,
+                 seed=5, splits=9),
     ]
 }
 

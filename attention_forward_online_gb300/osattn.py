@@ -24,7 +24,8 @@ ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
 ERR_TIMEOUT = 4
 
-EXPORTS = ("osattn_fwd", "osattn_status_string", "osattn_get_device_status",
+EXPORTS = ("osattn_fwd", "osattn_fwd_splitkv", "osattn_splitkv_workspace_bytes",
+           "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
 
@@ -52,6 +53,12 @@ def lib():
             L.osattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp, i32, vp]
             L.osattn_fwd.restype = i32
+            L.osattn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                             ctypes.c_float, i32, vp, i32, i32, vp,
+                                             ctypes.c_size_t, vp]
+            L.osattn_fwd_splitkv.restype = i32
+            L.osattn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.osattn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_status_string.argtypes = [i32]
             L.osattn_status_string.restype = ctypes.c_char_p
             L.osattn_get_device_status.argtypes = [vp]
@@ -130,6 +137,64 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, key_len=None,
                  B, H, Nq, Nkv, d, scale, causal, kl_ptr, dtype, _stream_handle(stream))
     if st != OK:
         raise OsattnError(st, "osattn_fwd")
+    return out, lse
+
+
+MAX_SPLITS = 128
+
+
+def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(lib().osattn_splitkv_workspace_bytes(int(B), int(H), int(Nq), int(d),
+                                                    int(num_splits)))
+
+
+def _check_qkv(q, k, v):
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be bf16 or all fp32")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
+        raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    return B, H, Nq, Nkv, d
+
+
+def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bool = False,
+                key_len=None, out=None, lse=None, workspace=None, stream=None):
+    """Split-KV attention forward (bf16): same result as fwd(), the key axis cut
+    into num_splits ranges merged by the (m, l) combine.  `workspace` may be a
+    preallocated CUDA uint8 tensor of at least splitkv_workspace_bytes(...)
+    bytes; otherwise torch allocates one."""
+    import torch
+
+    B, H, Nq, Nkv, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = splitkv_workspace_bytes(B, H, Nq, d, max(int(num_splits), 1))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    kl_ptr = None
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise ValueError("key_len must be a CUDA int32 tensor with B entries")
+        key_len = key_len.contiguous()
+        kl_ptr = key_len.data_ptr()
+    dtype = BF16 if q.dtype == torch.bfloat16 else FP32
+    st = lib().osattn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, Nq, Nkv, d, float(scale),
+                                  int(bool(causal)), kl_ptr, dtype, int(num_splits),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_fwd_splitkv")
     return out, lse
 
 

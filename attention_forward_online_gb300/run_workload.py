@@ -22,14 +22,19 @@ def main(argv=None):
     import torch
 
     from attention_forward_online_gb300 import osattn
-    from attention_forward_online_gb300.inputs import WORKLOADS, make_inputs
+    from attention_forward_online_gb300.inputs import SPLITKV_WORKLOADS, WORKLOADS, make_inputs
 
+    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS)
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", required=True, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", required=True, choices=sorted(allw))
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--heads", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=-1,
+                    help="key ranges for the split-KV entry point (0: unsplit; default: the workload's)")
     args = ap.parse_args(argv)
-    w = WORKLOADS[args.workload]
+    w = allw[args.workload]
+    if args.splits >= 0:
+        w = dataclasses.replace(w, splits=args.splits)
     if args.heads:
         w = dataclasses.replace(w, H=min(args.heads, w.H))
     q, k, v, kl = make_inputs(w)
@@ -39,12 +44,20 @@ def main(argv=None):
     O = torch.empty_like(qd)
     L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
     s = torch.cuda.Stream(device=dev)
+    ws = None
+    if w.splits:
+        ws = torch.empty(osattn.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, w.splits),
+                         dtype=torch.uint8, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.launches)]
     with torch.cuda.stream(s):
         for i in range(args.launches):
             ev[2 * i].record(s)
-            osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O, lse=L,
-                       stream=s)
+            if w.splits:
+                osattn.fwd_splitkv(qd, kd, vd, w.splits, scale=w.scale, causal=w.causal,
+                                   key_len=kld, out=O, lse=L, workspace=ws, stream=s)
+            else:
+                osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O,
+                           lse=L, stream=s)
             ev[2 * i + 1].record(s)
     s.synchronize()
     st = osattn.get_device_status(s)
@@ -54,7 +67,7 @@ def main(argv=None):
     ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.launches)]
     tf = [w.flops / (m * 1e-3) / 1e12 for m in ms]
     med = sorted(ms[1:] if len(ms) > 1 else ms)[len(ms[1:] if len(ms) > 1 else ms) // 2]
-    print(f"{w.name} H={w.H}: launches {args.launches}, median {med:.4f} ms = "
+    print(f"{w.name} H={w.H} splits={w.splits}: launches {args.launches}, median {med:.4f} ms = "
           f"{w.flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
           f"ms {['%.4f' % m for m in ms]}")
     return 0

@@ -264,10 +264,18 @@ def run_ours(args, w):
     L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    ws = None
+    if w.splits:
+        ws = torch.empty(osattn.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, w.splits),
+                         dtype=torch.uint8, device=dev)
 
     def step():
-        osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O, lse=L,
-                   stream=stream)
+        if w.splits:  # split-KV entry point: split kernel + combine kernel
+            osattn.fwd_splitkv(qd, kd, vd, w.splits, scale=w.scale, causal=w.causal,
+                               key_len=kld, out=O, lse=L, workspace=ws, stream=stream)
+        else:
+            osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O,
+                       lse=L, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
@@ -354,6 +362,7 @@ def run_ours(args, w):
             "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv,
                        "d": w.d, "causal": w.causal, "key_len": w.key_len,
+                       "splits": w.splits,
                        "flops_per_step": w.flops,
                        "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -364,7 +373,9 @@ def run_ours(args, w):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3),
                          "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "fwd_bf16_kernel" if w.dtype == "bf16" else "fwd_fp32_kernel",
+                         "kernel": ("fwd_bf16_kernel (split) + splitkv_combine_kernel, timed together"
+                                    if w.splits else
+                                    "fwd_bf16_kernel" if w.dtype == "bf16" else "fwd_fp32_kernel"),
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"},
             "cpu_baseline": {"value": round(cpu_tflops, 6), "unit": "TFLOPS",
                              "cores": cpu_cores(), "kind": "oracle",
@@ -373,7 +384,7 @@ def run_ours(args, w):
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if w.splits else 1),
             "clocks": clock_info,
             "kernel_source_sha": kernel_source_hash(),
         }
@@ -386,17 +397,18 @@ def run_ours(args, w):
 
 
 def main(argv=None):
-    from attention_forward_online_gb300.inputs import BENCH_WORKLOAD, WORKLOADS
+    from attention_forward_online_gb300.inputs import BENCH_WORKLOAD, SPLITKV_WORKLOADS, WORKLOADS
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
+    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS)
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(allw))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
-    w = WORKLOADS[args.workload]
+    w = allw[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

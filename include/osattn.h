@@ -19,6 +19,7 @@
 #ifndef OSATTN_H
 #define OSATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -87,6 +88,46 @@ extern "C" {
 int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                int B, int H, int Nq, int Nkv, int d, float scale, int causal,
                const int32_t* key_len, int dtype, void* stream);
+
+/* Largest num_splits osattn_fwd_splitkv accepts. */
+#define OSATTN_MAX_SPLITS 128
+
+/*
+ * osattn_splitkv_workspace_bytes - device workspace osattn_fwd_splitkv needs:
+ * num_splits * B*H*Nq * (d + 1) fp32 values (a normalised partial O row and
+ * its partial LSE per key range).  Returns 0 for sizes < 1.
+ */
+size_t osattn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * osattn_fwd_splitkv - the same result as osattn_fwd (same arguments,
+ * layouts, masking and fully-masked-row rule), computed with the key axis
+ * cut into num_splits ranges so that few (b, h) rows with long key sequences
+ * still fill the GPU.
+ *
+ * Each CTA runs the online-softmax loop over one key range and writes a
+ * partial O_s = O / l_s (fp32) and lse_s = m_s + ln l_s; a second kernel
+ * folds the partials of every row with the guarded (m, l) combine of [Ch6]
+ * §6.4.1 - the two-stage reduction [Ch6] §6.7.1 describes for a row split
+ * across blocks - and writes O (bf16) and LSE.  A key range with no visible
+ * key contributes the (-inf, 0) identity.
+ *
+ *   dtype            OSATTN_BF16 only (OSATTN_FP32 -> OSATTN_ERR_UNSUPPORTED)
+ *   num_splits       1 .. OSATTN_MAX_SPLITS (else OSATTN_ERR_INVALID_ARG); ranges are
+ *                    equal cuts of each 256-row query block's 128-key tiles, so
+ *                    splits beyond the tile count receive empty ranges
+ *   workspace        caller-owned device memory, 16-byte aligned, at least
+ *                    osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes
+ *                    (else OSATTN_ERR_INVALID_ARG); overwritten by the call and
+ *                    free for other use once the stream passes it
+ *
+ * Both kernels are enqueued on `stream`; the call allocates nothing.
+ * Errors as for osattn_fwd.
+ */
+int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       int B, int H, int Nq, int Nkv, int d, float scale, int causal,
+                       const int32_t* key_len, int dtype, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char* osattn_status_string(int status);

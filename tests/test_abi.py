@@ -89,3 +89,35 @@ def test_binding_rejects_cpu_tensors(L):
         osattn.fwd(q, q, q)
     with pytest.raises(TypeError):
         osattn.fwd(q, q.float(), q)
+
+
+def test_splitkv_workspace_size(L):
+    # num_splits * B*H*Nq * (d + 1) fp32 values
+    assert osattn.splitkv_workspace_bytes(1, 1, 4, 64, 2) == 2 * 4 * 65 * 4
+    assert osattn.splitkv_workspace_bytes(2, 3, 100, 128, 7) == 7 * 600 * 129 * 4
+    assert osattn.splitkv_workspace_bytes(0, 1, 4, 64, 2) == 0
+    assert osattn.splitkv_workspace_bytes(1, 1, 4, 64, 0) == 0
+
+
+def call_split(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, Nq=8, Nkv=8, d=64, scale=0.125, causal=0,
+             key_len=None, dtype=osattn.BF16, splits=2, ws=P, ws_bytes=1 << 20)
+    a.update(kw)
+    return osattn.lib().osattn_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                           a["H"], a["Nq"], a["Nkv"], a["d"], a["scale"],
+                                           a["causal"], a["key_len"], a["dtype"], a["splits"],
+                                           a["ws"], a["ws_bytes"], ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), osattn.ERR_INVALID_ARG),
+    (dict(splits=0), osattn.ERR_INVALID_ARG),
+    (dict(splits=129), osattn.ERR_INVALID_ARG),
+    (dict(ws=None), osattn.ERR_INVALID_ARG),
+    (dict(ws=P + 4), osattn.ERR_INVALID_ARG),
+    (dict(ws_bytes=2 * 8 * 65 * 4 - 1), osattn.ERR_INVALID_ARG),
+    (dict(dtype=osattn.FP32), osattn.ERR_UNSUPPORTED),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+])
+def test_splitkv_host_validation(L, kw, expect):
+    assert call_split(**kw) == expect
