@@ -116,6 +116,8 @@ const char* osattn_status_string(int status) {
     case OSATTN_ERR_UNSUPPORTED: return "unsupported head dimension or dtype";
     case OSATTN_ERR_CUDA: return "CUDA error";
     case OSATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case OSATTN_ERR_SCRATCH_LIMIT:
+      return "problem needs more split-KV scratch than the library's built-in array";
     default: return "unknown status";
   }
 }

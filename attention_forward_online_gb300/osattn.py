@@ -23,8 +23,11 @@ ERR_INVALID_ARG = 1
 ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
 ERR_TIMEOUT = 4
+ERR_SCRATCH_LIMIT = 5
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ("osattn_fwd", "osattn_fwd_splitkv", "osattn_splitkv_workspace_bytes",
+           "osattn_fwd_splitkv_noalloc",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -57,6 +60,9 @@ def lib():
                                              ctypes.c_float, i32, vp, i32, i32, vp,
                                              ctypes.c_size_t, vp]
             L.osattn_fwd_splitkv.restype = i32
+            L.osattn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                     ctypes.c_float, i32, vp, i32, i32, vp]
+            L.osattn_fwd_splitkv_noalloc.restype = i32
             L.osattn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             L.osattn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_status_string.argtypes = [i32]

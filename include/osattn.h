@@ -39,6 +39,8 @@ extern "C" {
 #define OSATTN_ERR_CUDA 3        /* a CUDA call failed (launch, attribute, tensor map) */
 #define OSATTN_ERR_TIMEOUT 4     /* a device-side wait ran past its limit (reported by
                                     osattn_get_device_status only) */
+#define OSATTN_ERR_SCRATCH_LIMIT 5 /* osattn_fwd_splitkv_noalloc: the problem's partials need
+                                      more than OSATTN_NOALLOC_SCRATCH_BYTES */
 
 /*
  * osattn_fwd - attention forward with online softmax.
@@ -128,6 +130,38 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        int B, int H, int Nq, int Nkv, int d, float scale, int causal,
                        const int32_t* key_len, int dtype, int num_splits, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/* Size of the scratch array built into the library for
+ * osattn_fwd_splitkv_noalloc (32 MiB on every GPU that loads the library). */
+#define OSATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * osattn_fwd_splitkv_noalloc - osattn_fwd_splitkv without a caller-provided
+ * workspace, for callers that cannot allocate device memory: an application
+ * whose own memory manager owns the device budget and forbids other
+ * allocations, or a latency-critical path that cannot pay for cudaMalloc's
+ * implicit synchronisation.  (The pages have no counterpart; this is an
+ * interface convenience, not part of the method.)
+ *
+ * Same arguments, results and errors as osattn_fwd_splitkv, minus the
+ * workspace: the partial results go to a fixed array of
+ * OSATTN_NOALLOC_SCRATCH_BYTES compiled into the library.  A problem with
+ * osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits) greater than that
+ * is rejected with OSATTN_ERR_SCRATCH_LIMIT before anything is enqueued;
+ * use fewer splits, or osattn_fwd_splitkv with your own workspace.
+ *
+ * The call allocates nothing.  Its first call on a device looks up that
+ * device's copy of the array (cudaGetSymbolAddress, with the device
+ * current); make that first call before any stream capture.  Every call on
+ * a device shares the one array and leaves its contents behind; nothing in
+ * it has to start at zero.  Calls whose kernels can overlap on the GPU (for
+ * example on two streams without ordering between them) race on the array
+ * and give undefined results: order them on one stream or with events.
+ */
+int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
+                               float* LSE, int B, int H, int Nq, int Nkv, int d, float scale,
+                               int causal, const int32_t* key_len, int dtype, int num_splits,
+                               void* stream);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char* osattn_status_string(int status);

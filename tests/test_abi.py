@@ -121,3 +121,13 @@ def call_split(**kw):
 ])
 def test_splitkv_host_validation(L, kw, expect):
     assert call_split(**kw) == expect
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(L):
+    # 4 x 8 x 4096 rows x 129 floats x 4 splits > 32 MiB: rejected on the host
+    need = osattn.splitkv_workspace_bytes(4, 8, 4096, 128, 4)
+    assert need > osattn.NOALLOC_SCRATCH_BYTES
+    rc = L.osattn_fwd_splitkv_noalloc(P, P, P, P, P, 4, 8, 4096, 4096, 128, 0.125, 0, None,
+                                      osattn.BF16, 4, ctypes.c_void_p(None))
+    assert rc == osattn.ERR_SCRATCH_LIMIT
+    assert "scratch" in osattn.status_string(rc)
