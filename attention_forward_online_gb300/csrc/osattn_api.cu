@@ -245,6 +245,22 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
   return launch_splitkv(a, num_splits, o_part, lse_part);
 }
 
+int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,
+                        void* stream) {
+  if (!in || !out || rows < 1 || N < 1) return OSATTN_ERR_INVALID_ARG;
+  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
+  const uintptr_t el = dtype == OSATTN_BF16 ? 2 : 4;
+  if (!aligned(in, el) || !aligned(out, el) || (lse && !aligned(lse, 4)))
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  const cudaError_t e = osattn::launch_softmax_rows(in, out, lse, static_cast<long long>(rows), N,
+                                                    dtype == OSATTN_FP32, st->num_sms,
+                                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
 int osattn_get_device_status(void* stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st);

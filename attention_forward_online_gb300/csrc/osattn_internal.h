@@ -45,6 +45,10 @@ cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, v
                                    float* LSE, long long rows, int d, int num_splits,
                                    cudaStream_t stream);
 
+// Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix.
+cudaError_t launch_softmax_rows(const void* in, void* out, float* lse, long long rows, int N,
+                                int dtype_fp32, int num_sms, cudaStream_t stream);
+
 // Box shape the bf16 kernel expects in its tensor maps.
 constexpr int kBoxInner = 64;   // elements along d (128 bytes)
 constexpr int kBoxRows = 128;   // rows of Q / K / V

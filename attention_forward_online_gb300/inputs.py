@@ -77,6 +77,47 @@ SPLITKV_WORKLOADS = {
     ]
 }
 
+@dataclasses.dataclass(frozen=True)
+class RowWorkload:
+    """A [rows, N] matrix of logits for the standalone row softmax."""
+    name: str
+    dtype: str
+    rows: int
+    N: int
+    seed: int
+    std: float = 3.0
+
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    @property
+    def bytes_moved(self) -> int:
+        """Read once + write once per element, plus the fp32 LSE per row."""
+        return self.rows * self.N * self.elem_bytes * 2 + self.rows * 4
+
+
+# The chapter's exercise is a whole-row softmax at N = 4096; 65536 such rows
+# (512 MiB of bf16 each way) keep every SM streaming and exceed L2.
+ROW_WORKLOADS = {
+    w.name: w
+    for w in [
+        RowWorkload("softmax_rows_bf16_r65536_n4096", "bf16", 65536, 4096, seed=6),
+        RowWorkload("softmax_rows_fp32_r32768_n4096", "fp32", 32768, 4096, seed=7),
+    ]
+}
+
+
+def make_rows(w: RowWorkload):
+    """Logits [rows, N] ~ N(0, std^2) on the CPU, rounded to the dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    return (torch.randn((w.rows, w.N), generator=g, dtype=torch.float32) * w.std).to(w.torch_dtype())
+
+
 # The workload the benchmark times by default: the largest bf16 one.
 BENCH_WORKLOAD = "bf16_causal_b1_h32_n16384_d128_qstd3"
 

@@ -27,7 +27,7 @@ ERR_SCRATCH_LIMIT = 5
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ("osattn_fwd", "osattn_fwd_splitkv", "osattn_splitkv_workspace_bytes",
-           "osattn_fwd_splitkv_noalloc",
+           "osattn_fwd_splitkv_noalloc", "osattn_softmax_rows",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -63,6 +63,8 @@ def lib():
             L.osattn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      ctypes.c_float, i32, vp, i32, i32, vp]
             L.osattn_fwd_splitkv_noalloc.restype = i32
+            L.osattn_softmax_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, vp]
+            L.osattn_softmax_rows.restype = i32
             L.osattn_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             L.osattn_splitkv_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_status_string.argtypes = [i32]
@@ -201,6 +203,28 @@ def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bo
                                   _stream_handle(stream))
     if st != OK:
         raise OsattnError(st, "osattn_fwd_splitkv")
+    return out, lse
+
+
+def softmax_rows(x, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Row softmax of a contiguous CUDA [rows, N] bf16/fp32 tensor (online (m, l)
+    normaliser).  Returns (y, lse or None); `out` may be `x` (in place)."""
+    import torch
+
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA [rows, N] tensor")
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bf16 or fp32")
+    rows, N = x.shape
+    out = torch.empty_like(x) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=x.device)
+    dtype = BF16 if x.dtype == torch.bfloat16 else FP32
+    st = lib().osattn_softmax_rows(x.data_ptr(), out.data_ptr(),
+                                   None if lse is None else lse.data_ptr(), rows, N, dtype,
+                                   _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_softmax_rows")
     return out, lse
 
 

@@ -396,8 +396,127 @@ def run_ours(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ row softmax
+def run_softmax_rows(args, w):
+    """The standalone online row softmax: HBM-bound, one read and one write
+    per element; value = bytes moved / kernel time."""
+    import numpy as np
+    import torch
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import make_rows
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    x = make_rows(w)
+    xd = x.to(dev)
+    yd = torch.empty_like(xd)
+    ld = torch.empty(w.rows, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        osattn.softmax_rows(xd, out=yd, lse=ld, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    barrier(world)
+    local_ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    total_ms = reduce_max(local_ms, world)
+    gbs = world * w.bytes_moved * args.steps / (total_ms * 1e-3) / 1e9
+    achieved = w.bytes_moved / (local_ms / args.steps * 1e-3) / 1e9
+
+    xh = x.pin_memory()
+    yh = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    lh = torch.empty(w.rows, dtype=torch.float32).pin_memory()
+    n_e2e = max(3, min(args.steps, 20))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            es[i].record(stream)
+            xd.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(yd, non_blocking=True)
+            lh.copy_(ld, non_blocking=True)
+            ee[i].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(sum(s_.elapsed_time(e_) for s_, e_ in zip(es, ee)), world) / n_e2e
+    if rank == 0:
+        import oracle
+
+        rng = np.random.default_rng(9)
+        n_rows = 64
+        while True:  # bounded sample: grow until the oracle takes ~args.cpu_seconds
+            rows = np.sort(rng.choice(w.rows, size=min(n_rows, w.rows), replace=False))
+            t0 = time.perf_counter()
+            Yr, Lr = oracle.softmax_rows(x[torch.from_numpy(rows)])
+            secs = time.perf_counter() - t0
+            if secs >= args.cpu_seconds / 4 or n_rows >= w.rows:
+                break
+            n_rows = min(w.rows, int(n_rows * max(2.0, args.cpu_seconds / 4 / max(secs, 1e-3))))
+        cpu_gbs = len(rows) * (w.N * w.elem_bytes * 2 + 4) / secs / 1e9
+        Yg = yd[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        Lg = ld[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        fin = np.isfinite(Lr)
+        peak = float(peaks["hbm_gbs"])
+        line = {
+            "metric": "online row softmax HBM GB/s (one read + one write per element)",
+            "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "rows": w.rows, "N": w.N,
+                       "bytes_per_step": w.bytes_moved,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "max_abs_err": {"y": float(np.abs(Yg - Yr).max()),
+                            "LSE": float(np.abs(Lg[fin] - Lr[fin]).max()),
+                            "rows_checked": int(len(rows))},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "softmax_rows_regs",
+                         "peak_source": f"hbm_gbs (copy) of {peak_src}"},
+            "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cpu_cores(),
+                             "kind": "oracle",
+                             "sample": f"{len(rows)} random rows of {w.name}, fp64, {secs:.1f} s"},
+            "e2e": {"value": round(world * w.bytes_moved / (e2e_ms * 1e-3) / 1e9, 2),
+                    "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+                    "d2h_bytes_per_step": yh.numel() * yh.element_size() + lh.numel() * 4,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps, "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
-    from attention_forward_online_gb300.inputs import BENCH_WORKLOAD, SPLITKV_WORKLOADS, WORKLOADS
+    from attention_forward_online_gb300.inputs import (BENCH_WORKLOAD, ROW_WORKLOADS,
+                                                       SPLITKV_WORKLOADS, WORKLOADS)
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,9 +524,16 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     allw = dict(WORKLOADS, **SPLITKV_WORKLOADS)
-    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(allw))
+    ap.add_argument("--workload", default=BENCH_WORKLOAD,
+                    choices=sorted(allw) + sorted(ROW_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
+    if args.workload in ROW_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the reference arm is defined for the attention workloads"}))
+            return 0
+        return run_softmax_rows(args, ROW_WORKLOADS[args.workload])
     w = allw[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -163,6 +163,27 @@ int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void
                                int causal, const int32_t* key_len, int dtype, int num_splits,
                                void* stream);
 
+/*
+ * osattn_softmax_rows - row softmax of a [rows, N] matrix with the online
+ * (m, l) normaliser of [Ch6] §6.4: per row,
+ *     y_i = e^{x_i - m} / l,  m = max_i x_i,  l = sum_i e^{x_i - m},
+ *     LSE = m + ln l                                          ([Ch6] §6.5)
+ * with per-thread states merged by the guarded combine of [Ch6] §6.4.1.
+ * Rows of up to 32768 elements are held in registers: read once and written
+ * once; longer rows are read twice.  -inf entries act as the additive mask
+ * of [Ch6] §6.7.3; a row of only -inf gives y = 0 and LSE = -inf (no NaN).
+ *
+ *   in, out  device, [rows, N] contiguous, element type `dtype` (bf16 or fp32);
+ *            element-aligned; in == out (in place) is allowed
+ *   lse      device fp32 [rows], or NULL to skip it
+ *   rows, N  >= 1
+ *   stream   cudaStream_t (NULL: legacy default stream)
+ * Errors: OSATTN_ERR_INVALID_ARG (null/size/alignment), OSATTN_ERR_UNSUPPORTED
+ * (dtype), OSATTN_ERR_CUDA (launch).  Asynchronous like osattn_fwd.
+ */
+int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,
+                        void* stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char* osattn_status_string(int status);
 

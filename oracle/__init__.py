@@ -61,6 +61,8 @@ def _load():
             vp, vp, vp, ctypes.c_int, dp, dp,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_int, vp, vp, ctypes.c_int64, ctypes.c_int]
+        lib.osattn_ref_softmax_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                dp, dp, ctypes.c_int]
         lib.osattn_ref_attention_blocked.argtypes = [
             vp, vp, vp, ctypes.c_int, dp, dp,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -183,6 +185,22 @@ def attention_fwd(Q, K, V, scale: float, causal: bool = False, key_len=None,
     if rc:
         raise ValueError("invalid arguments to the oracle")
     return O, L
+
+
+def softmax_rows(X, nthreads: int = 0):
+    """Row softmax of a [rows, N] tensor (torch bf16/fp32/fp64 or numpy
+    fp32/fp64) by the three-pass safe softmax, row by row (ch. 6 §6.2); also
+    returns the row LSE (§6.5).  All -inf rows give y = 0, LSE = -inf."""
+    x, dt = _as_raw(X)
+    if x.ndim != 2:
+        raise ValueError("X must be [rows, N]")
+    rows, N = x.shape
+    Y = np.empty((rows, N))
+    L = np.empty(rows)
+    if _load().osattn_ref_softmax_rows(x.ctypes.data, dt, rows, N, _dptr(Y), _dptr(L),
+                                       int(nthreads)):
+        raise ValueError("invalid arguments to the oracle")
+    return Y, L
 
 
 def attention_blocked(Q, K, V, scale: float, causal: bool = False, key_len=None,

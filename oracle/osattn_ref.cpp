@@ -235,6 +235,28 @@ double osattn_ref_lse(double m, double l) {
   return m + std::log(l);
 }
 
+// Row softmax of a [rows, N] matrix by the three-pass safe softmax of
+// [Ch6] §6.2, row by row: y = e^{x - m} / l with m = max x, l = sum e^{x - m},
+// and lse = m + log l ([Ch6] §6.5).  A row of only -inf (all masked) has no
+// defined softmax; it yields y = 0 and lse = -inf.  x is bf16 bits, fp32 or
+// fp64 (dtype 0/1/2); y and lse are double; lse may be null.
+int osattn_ref_softmax_rows(const void* x, int dtype, int64_t rows, int N, double* y,
+                            double* lse, int nthreads) {
+  if (!x || !y || rows < 1 || N < 1 || dtype < REF_BF16 || dtype > REF_FP64) return 1;
+  parallel_rows(rows, nthreads, [&](int64_t r) {
+    const int64_t base = r * N;
+    double m = kNegInf;
+    for (int i = 0; i < N; ++i) m = std::max(m, load_elem(x, dtype, base + i));
+    double l = 0.0;
+    if (m != kNegInf)
+      for (int i = 0; i < N; ++i) l += std::exp(load_elem(x, dtype, base + i) - m);
+    for (int i = 0; i < N; ++i)
+      y[base + i] = (m == kNegInf) ? 0.0 : std::exp(load_elem(x, dtype, base + i) - m) / l;
+    if (lse) lse[r] = (m == kNegInf) ? kNegInf : m + std::log(l);
+  });
+  return 0;
+}
+
 // Attention forward by the definition in the file header.
 //   Q: [B,H,Nq,d], K/V: [B,H,Nkv,d], contiguous, element format `dtype`
 //   (0 bf16 bits, 1 fp32, 2 fp64).  key_len: host int32 [B] or null.

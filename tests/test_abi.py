@@ -131,3 +131,15 @@ def test_noalloc_rejects_problems_beyond_its_scratch(L):
                                       osattn.BF16, 4, ctypes.c_void_p(None))
     assert rc == osattn.ERR_SCRATCH_LIMIT
     assert "scratch" in osattn.status_string(rc)
+
+
+def test_softmax_rows_host_validation(L):
+    f = L.osattn_softmax_rows
+    nul = ctypes.c_void_p(None)
+    assert f(None, P, None, 4, 8, osattn.BF16, nul) == osattn.ERR_INVALID_ARG
+    assert f(P, P, None, 0, 8, osattn.BF16, nul) == osattn.ERR_INVALID_ARG
+    assert f(P, P, None, 4, 0, osattn.BF16, nul) == osattn.ERR_INVALID_ARG
+    assert f(P + 1, P, None, 4, 8, osattn.BF16, nul) == osattn.ERR_INVALID_ARG
+    assert f(P, P + 2, None, 4, 8, osattn.FP32, nul) == osattn.ERR_INVALID_ARG
+    assert f(P, P, P + 2, 4, 8, osattn.FP32, nul) == osattn.ERR_INVALID_ARG
+    assert f(P, P, None, 4, 8, 9, nul) == osattn.ERR_UNSUPPORTED

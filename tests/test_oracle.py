@@ -348,3 +348,22 @@ def test_oracle_rejects_bad_arguments(ref):
         ref.attention_fwd(q, q, q, 1.0, rows=[5])
     with pytest.raises(ValueError):
         ref.attention_fwd(q, np.zeros((1, 1, 2, 3)), q, 1.0)
+
+
+# ---------------------------------------------------------------- batched row softmax
+@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16])
+def test_softmax_rows_matches_scipy_and_worked_example(ref, golden, dtype):
+    g = torch.Generator().manual_seed(21)
+    X = (torch.randn(37, 301, generator=g, dtype=torch.float64) * 5).to(dtype)
+    X[3, :50] = -float("inf")           # leading masked run
+    X[7, :] = -float("inf")             # fully masked row
+    X[9, 0] = golden["x"][0]
+    Y, L = ref.softmax_rows(X)
+    x = X.double().numpy()
+    live = np.isfinite(x).any(axis=1)
+    np.testing.assert_allclose(Y[live], scipy.special.softmax(x[live], axis=1), rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(L[live], scipy.special.logsumexp(x[live], axis=1), atol=1e-12)
+    assert np.all(Y[~live] == 0.0) and np.all(L[~live] == -np.inf)
+    assert np.allclose(Y[live].sum(axis=1), 1.0, atol=1e-12)
+    Yw, Lw = ref.softmax_rows(np.array([golden["x"]]))
+    np.testing.assert_allclose(Yw[0], golden["y"], atol=golden["tol"])
