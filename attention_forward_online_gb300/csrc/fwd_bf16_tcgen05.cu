@@ -12,6 +12,11 @@
 // Exponentials run in base 2 with scale * log2(e) folded into one FMA; m and
 // l live in those units and LSE converts back to natural log.
 //
+// Element type: bf16 or IEEE fp16 (template kF16), the same for Q, K, V, P
+// and O; the MMAs accumulate in fp32 either way.  Q, K and V are read through
+// 4-D tensor maps (d, N, H, B) with the caller's strides and O is written
+// through its own strides, so [B, N, H, d] tensors need no transposing copy.
+//
 // CTA layout: 512 threads own two 128-row query tiles (Q0, Q1) of one (b, h)
 // and stream that head's K/V tiles once for both.
 //   warps 0-3   softmax for tile 0, one query row per thread (tensor-memory
@@ -97,7 +102,8 @@ constexpr int smem_bytes() {
 }
 
 struct Params {
-  __nv_bfloat16* O;
+  uint16_t* O;      // bf16 or fp16 elements
+  long long o_sb, o_sh, o_sn;  // O strides (elements) of the b, h and row axes
   float* LSE;
   float* o_part;    // split-KV only: [splits, B*H, Nq, d] fp32 partial O (already / l_s)
   float* lse_part;  // split-KV only: [splits, B*H, Nq] fp32 partial LSE
@@ -126,6 +132,13 @@ __device__ __forceinline__ void regs_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packs two fp32 values into the kernel's 16-bit element type.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kF16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
 }
 
 // Number of K/V tiles a query tile starting at row q0 must visit: keys
@@ -165,10 +178,11 @@ __device__ __forceinline__ float min128(const uint32_t* v) {
 
 // ------------------------------------------------------------------ softmax
 // One thread per query row of tile t (tensor-memory lane = row).
-template <int HD, bool kSplit>
+template <int HD, bool kSplit, bool kF16>
 __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32_t tmem, int t,
-                                             int bh, int q0, int n_t, int kv_len, int sb,
+                                             int b, int h, int q0, int n_t, int kv_len, int sb,
                                              int split, WaitCtl wc) {
+  const int bh = b * p.H + h;
   using C = Cfg<HD>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter+32)
@@ -219,11 +233,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     const uint64_t cm2 = f2_pack(cm, cm), nm2 = f2_pack(neg_m, neg_m);
     uint64_t rs_a = 0, rs_b = 0;  // packed partial row sums (bit pattern 0 = 0.0f)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int half = 0; half < 2; ++half) {
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const int i = h * 64 + 2 * e;
+        const int i = half * 64 + 2 * e;
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), cm2, nm2),
                   x0, x1);
@@ -233,9 +247,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
           rs_b = f2_add(rs_b, pp);
         else
           rs_a = f2_add(rs_a, pp);
-        pk[e] = pack_bf16x2(p0, p1);
+        pk[e] = pack2<kF16>(p0, p1);
       }
-      tmem_st_32x32b_x32(s_addr + h * 32, pk);
+      tmem_st_32x32b_x32(s_addr + half * 32, pk);
     }
     float r0, r1, r2, r3;
     f2_unpack(rs_a, r0, r1);
@@ -288,7 +302,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
   }
   const uint64_t inv2 = f2_pack(inv_l, inv_l);
   const bool store = qi < p.Nq;
-  __nv_bfloat16* orow = p.O + (static_cast<long long>(bh) * p.Nq + qi) * HD;
+  uint16_t* orow = p.O + b * p.o_sb + h * p.o_sh + qi * p.o_sn;
   const uint32_t o_addr = lane_base + C::kOCol0 + static_cast<uint32_t>(t * HD);
 #pragma unroll
   for (int ch = 0; ch < HD / 32; ++ch) {
@@ -307,7 +321,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
       float a0, a1;
       f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[2 * e]), __uint_as_float(orr[2 * e + 1])), inv2),
                 a0, a1);
-      packed[e] = pack_bf16x2(a0, a1);
+      packed[e] = pack2<kF16>(a0, a1);
     }
     if (store) {
       uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
@@ -379,20 +393,20 @@ __device__ __forceinline__ void correction_role(Bars* bars, uint32_t tmem, int n
 template <int HD>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, Bars* bars, uint8_t* sQ,
-                                              uint8_t* sKV, int bh, int q0, int n0, int n1,
+                                              uint8_t* sKV, int b, int h, int q0, int n0, int n1,
                                               int sb, WaitCtl wc) {
   using C = Cfg<HD>;
   if (n0 > 0) {
     mbar_arrive_expect_tx(&bars->q_full[0], C::kQBytes);
 #pragma unroll
     for (int cb = 0; cb < HD / 64; ++cb)
-      tma_load_3d(sQ + cb * BM * 128, tmQ, &bars->q_full[0], cb * 64, q0, bh);
+      tma_load_4d(sQ + cb * BM * 128, tmQ, &bars->q_full[0], cb * 64, q0, h, b);
   }
   if (n1 > 0) {
     mbar_arrive_expect_tx(&bars->q_full[1], C::kQBytes);
 #pragma unroll
     for (int cb = 0; cb < HD / 64; ++cb)
-      tma_load_3d(sQ + C::kQBytes + cb * BM * 128, tmQ, &bars->q_full[1], cb * 64, q0 + BM, bh);
+      tma_load_4d(sQ + C::kQBytes + cb * BM * 128, tmQ, &bars->q_full[1], cb * 64, q0 + BM, h, b);
   }
   const int total = 2 * max(n0, n1);  // K_0, V_0, K_1, V_1, ...
   int u = 0;
@@ -405,7 +419,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
     const CUtensorMap* map = (u & 1) ? tmV : tmK;
 #pragma unroll
     for (int cb = 0; cb < HD / 64; ++cb)
-      tma_load_3d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (sb + (u >> 1)) * BN, bh);
+      tma_load_4d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (sb + (u >> 1)) * BN, h, b);
   }
   // Let every load this thread issued land before the CTA can exit.
   if (n0 > 0) drain_wait(&bars->q_full[0], 0, wc.limit_ns);
@@ -419,9 +433,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 // S_t = Q_t K^T: 128 x 128 fp32 into tensor-memory columns [t*128, t*128+128).
 // a_desc / b_desc address the first 16-element K slice; later slices move 32
 // bytes within a 128-byte swizzle row, or to the next 64-column block.
-template <int HD>
+template <int HD, bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
-  constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);  // K-major A and B
+  constexpr uint32_t idS = idesc_f16_f32(BM, BN, 0, kF16);  // K-major A and B
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
@@ -431,17 +445,17 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a_desc, uint64
 
 // O_t (+)= P_t V: P from tensor memory (bf16 pairs over S_t), V MN-major in
 // shared memory; 16 keys per step = two 8-row swizzle atoms (2 KB).
-template <int HD>
+template <int HD, bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
-  constexpr uint32_t idPV = idesc_bf16_f32(BM, HD, 1);  // B (V) is MN-major
+  constexpr uint32_t idPV = idesc_f16_f32(BM, HD, 1, kF16);  // B (V) is MN-major
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
     mma_bf16_ts(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int HD>
+template <int HD, bool kF16>
 __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ, uint8_t* sKV,
                                          int n0, int n1, WaitCtl wc) {
   using C = Cfg<HD>;
@@ -479,11 +493,11 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       ok = mbar_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
       if (!ok) break;
       tc_fence_after_sync();
-      issue_pv<HD>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
+      issue_pv<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
       mma_commit(&bars->o_full[0]);
     }
     if (j < n0) {
-      issue_s<HD>(s_col0, q_desc0, k_desc + ks * kStageStep);
+      issue_s<HD, kF16>(s_col0, q_desc0, k_desc + ks * kStageStep);
       mma_commit(&bars->s_full[0]);
     }
     // tile 1: PV1(j-1), then S1(j)
@@ -491,11 +505,11 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       ok = mbar_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
       if (!ok) break;
       tc_fence_after_sync();
-      issue_pv<HD>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
+      issue_pv<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
       mma_commit(&bars->o_full[1]);
     }
     if (j < n1) {
-      issue_s<HD>(s_col1, q_desc1, k_desc + ks * kStageStep);
+      issue_s<HD, kF16>(s_col1, q_desc1, k_desc + ks * kStageStep);
       mma_commit(&bars->s_full[1]);
     }
     if (j > 0) mma_commit(&bars->kv_empty[vs]);
@@ -506,7 +520,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
   drain_wait(&bars->mma_drain, 0, wc.limit_ns);
 }
 
-template <int HD, bool kSplit>
+template <int HD, bool kSplit, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -530,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = unit / p.num_q_blocks;
   int qb = unit % p.num_q_blocks;
   if (p.causal) qb = p.num_q_blocks - 1 - qb;
-  const int b = bh / p.H;
+  const int b = bh / p.H, h = bh % p.H;
   int kv_len = p.Nkv;
   if (p.key_len) kv_len = min(max(p.key_len[b], 0), p.Nkv);
   const int q0 = qb * (kQTiles * BM);
@@ -583,16 +597,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kCorrWarp0) {
     regs_inc<184>();
     const int t = warp >> 2;
-    softmax_role<HD, kSplit>(p, bars, tmem, t, bh, q0 + t * BM, t ? n1 : n0, kv_len, sb, split, wc);
+    softmax_role<HD, kSplit, kF16>(p, bars, tmem, t, b, h, q0 + t * BM, t ? n1 : n0, kv_len, sb,
+                                   split, wc);
   } else if (warp < kProducerWarp) {
     regs_dec<88>();
     correction_role<HD>(bars, tmem, n0, n1, wc);
   } else {
     regs_dec<56>();
     if (warp == kProducerWarp && lane == 0 && n > 0)
-      producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, bh, q0, n0, n1, sb, wc);
+      producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, b, h, q0, n0, n1, sb, wc);
     else if (warp == kMmaWarp && lane == 0 && n > 0)
-      mma_role<HD>(bars, tmem, sQ, sKV, n0, n1, wc);
+      mma_role<HD, kF16>(bars, tmem, sQ, sKV, n0, n1, wc);
   }
 
   __syncwarp();
@@ -611,30 +626,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 // forever, so such a build is refused here instead of launched.
 constexpr int kLaunchRegs = 128;
 
-template <int HD, bool kSplit>
+template <int HD, bool kSplit, bool kF16>
 cudaError_t set_attrs() {
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<HD, kSplit>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, fwd_bf16_kernel<HD, kSplit, kF16>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(fwd_bf16_kernel<HD, kSplit>,
+  return cudaFuncSetAttribute(fwd_bf16_kernel<HD, kSplit, kF16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<HD>());
+}
+
+template <int HD, bool kSplit, bool kF16>
+void launch_one(dim3 g, dim3 blk, cudaStream_t s, const CUtensorMap& q, const CUtensorMap& k,
+                const CUtensorMap& v, const Params& p) {
+  fwd_bf16_kernel<HD, kSplit, kF16><<<g, blk, smem_bytes<HD>(), s>>>(q, k, v, p);
 }
 
 }  // namespace
 
 cudaError_t prepare_fwd_bf16() {
   cudaError_t e;
-  if ((e = set_attrs<64, false>()) != cudaSuccess) return e;
-  if ((e = set_attrs<128, false>()) != cudaSuccess) return e;
-  if ((e = set_attrs<64, true>()) != cudaSuccess) return e;
-  return set_attrs<128, true>();
+  if ((e = set_attrs<64, false, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<128, false, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<64, true, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<128, true, false>()) != cudaSuccess) return e;
+  if ((e = set_attrs<64, false, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<128, false, true>()) != cudaSuccess) return e;
+  if ((e = set_attrs<64, true, true>()) != cudaSuccess) return e;
+  return set_attrs<128, true, true>();
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV) {
   Params p;
-  p.O = static_cast<__nv_bfloat16*>(a.O);
+  p.O = static_cast<uint16_t*>(a.O);
+  p.o_sb = a.o_strides[0];
+  p.o_sh = a.o_strides[1];
+  p.o_sn = a.o_strides[2];
   p.LSE = a.LSE;
   p.o_part = a.o_part;
   p.lse_part = a.lse_part;
@@ -649,20 +677,20 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
   p.causal = a.causal;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
-  const bool split = a.num_splits > 0;
+  const bool split = a.num_splits > 0, f16 = a.fp16 != 0;
   const long long grid = static_cast<long long>(p.num_q_blocks) * a.B * a.H * p.num_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid)), blk(kThreads);
   if (a.d == 64) {
-    if (split)
-      fwd_bf16_kernel<64, true><<<g, blk, smem_bytes<64>(), a.stream>>>(tmQ, tmK, tmV, p);
-    else
-      fwd_bf16_kernel<64, false><<<g, blk, smem_bytes<64>(), a.stream>>>(tmQ, tmK, tmV, p);
+    if (f16) split ? launch_one<64, true, true>(g, blk, a.stream, tmQ, tmK, tmV, p)
+                   : launch_one<64, false, true>(g, blk, a.stream, tmQ, tmK, tmV, p);
+    else split ? launch_one<64, true, false>(g, blk, a.stream, tmQ, tmK, tmV, p)
+               : launch_one<64, false, false>(g, blk, a.stream, tmQ, tmK, tmV, p);
   } else {
-    if (split)
-      fwd_bf16_kernel<128, true><<<g, blk, smem_bytes<128>(), a.stream>>>(tmQ, tmK, tmV, p);
-    else
-      fwd_bf16_kernel<128, false><<<g, blk, smem_bytes<128>(), a.stream>>>(tmQ, tmK, tmV, p);
+    if (f16) split ? launch_one<128, true, true>(g, blk, a.stream, tmQ, tmK, tmV, p)
+                   : launch_one<128, false, true>(g, blk, a.stream, tmQ, tmK, tmV, p);
+    else split ? launch_one<128, true, false>(g, blk, a.stream, tmQ, tmK, tmV, p)
+               : launch_one<128, false, false>(g, blk, a.stream, tmQ, tmK, tmV, p);
   }
   return cudaGetLastError();
 }

@@ -9,9 +9,11 @@
 // fused additive mask (§6.7.3), and LSE = m + log l (§6.5).
 //
 // Work split: one CTA of 4 warps owns 16 query rows of one (b, h); each warp
-// owns 4 rows.  Keys stream through shared memory 32 at a time; lane j scores
-// key j against the warp's rows, the warp reduces the tile max and sum with
-// shuffles, and each lane accumulates d/32 output columns.
+// owns 4 rows.  Keys stream through shared memory 32 at a time; lane j
+// scores key j against the warp's rows, the warp reduces the tile max and sum
+// with shuffles, and each lane accumulates d/32 output columns.  Q, K, V and
+// O are addressed through element strides of their (b, h, row) axes, each a
+// multiple of 4 so every row stays 16-byte aligned.
 #include <cmath>
 #include <cstdint>
 
@@ -25,6 +27,10 @@ constexpr int kRowsPerWarp = 4;
 constexpr int kKeysPerTile = 32;
 constexpr unsigned kFull = 0xffffffffu;
 
+struct Strides {
+  long long q[3], k[3], v[3], o[3];  // element strides of (b, h, row)
+};
+
 template <int HD>
 __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__ Q,
                                                        const float* __restrict__ K,
@@ -33,7 +39,8 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
                                                        float* __restrict__ LSE,
                                                        const int32_t* __restrict__ key_len,
                                                        int H, int Nq, int Nkv, float scale,
-                                                       int causal, int num_q_tiles) {
+                                                       int causal, int num_q_tiles,
+                                                       const Strides st) {
   constexpr int CPL = HD / 32;  // output columns per lane
   __shared__ float sQ[kRowsPerCta][HD];
   __shared__ float sK[kKeysPerTile][HD + 1];  // +1: lane j reads row j conflict-free
@@ -43,21 +50,21 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
   const long long bh = blockIdx.x / num_q_tiles;
   int qt = blockIdx.x % num_q_tiles;
   if (causal) qt = num_q_tiles - 1 - qt;  // heaviest query tiles of a head first
-  const int b = static_cast<int>(bh / H);
+  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
   int kv_len = Nkv;
   if (key_len) kv_len = min(max(key_len[b], 0), Nkv);
   const int q0 = qt * kRowsPerCta;
   int kv_end = kv_len;
   if (causal) kv_end = min(kv_end, q0 + kRowsPerCta);
 
-  const float* Qbh = Q + bh * static_cast<long long>(Nq) * HD;
-  const float* Kbh = K + bh * static_cast<long long>(Nkv) * HD;
-  const float* Vbh = V + bh * static_cast<long long>(Nkv) * HD;
+  const float* Qbh = Q + b * st.q[0] + h * st.q[1];
+  const float* Kbh = K + b * st.k[0] + h * st.k[1];
+  const float* Vbh = V + b * st.v[0] + h * st.v[1];
 
   for (int e = threadIdx.x; e < kRowsPerCta * HD / 4; e += blockDim.x) {
     const int r = (e * 4) / HD, c = (e * 4) % HD;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q0 + r < Nq) v = *reinterpret_cast<const float4*>(Qbh + static_cast<long long>(q0 + r) * HD + c);
+    if (q0 + r < Nq) v = *reinterpret_cast<const float4*>(Qbh + (q0 + r) * st.q[2] + c);
     *reinterpret_cast<float4*>(&sQ[r][c]) = v;
   }
 
@@ -76,8 +83,8 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
       const int r = (e * 4) / HD, c = (e * 4) % HD;
       float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
       if (k0 + r < Nkv) {
-        kv = *reinterpret_cast<const float4*>(Kbh + static_cast<long long>(k0 + r) * HD + c);
-        vv = *reinterpret_cast<const float4*>(Vbh + static_cast<long long>(k0 + r) * HD + c);
+        kv = *reinterpret_cast<const float4*>(Kbh + (k0 + r) * st.k[2] + c);
+        vv = *reinterpret_cast<const float4*>(Vbh + (k0 + r) * st.v[2] + c);
       }
       sK[r][c] = kv.x; sK[r][c + 1] = kv.y; sK[r][c + 2] = kv.z; sK[r][c + 3] = kv.w;
       *reinterpret_cast<float4*>(&sV[r][c]) = vv;
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
     const int qi = q0 + warp * kRowsPerWarp + rr;
     if (qi >= Nq) continue;
     const float inv_l = l[rr] > 0.f ? 1.f / l[rr] : 0.f;
-    float* orow = O + (bh * Nq + qi) * static_cast<long long>(HD);
+    float* orow = O + b * st.o[0] + h * st.o[1] + qi * st.o[2];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) orow[lane + 32 * c] = o[rr][c] * inv_l;
     if (lane == 0) LSE[bh * Nq + qi] = l[rr] > 0.f ? m[rr] + logf(l[rr]) : -INFINITY;
@@ -182,12 +189,19 @@ cudaError_t launch_fwd_fp32(const FwdArgs& a) {
   const float* k = static_cast<const float*>(a.K);
   const float* v = static_cast<const float*>(a.V);
   float* o = static_cast<float*>(a.O);
+  Strides st;
+  for (int i = 0; i < 3; ++i) {
+    st.q[i] = a.q_strides[i];
+    st.k[i] = a.k_strides[i];
+    st.v[i] = a.v_strides[i];
+    st.o[i] = a.o_strides[i];
+  }
   if (a.d == 64)
     fwd_fp32_kernel<64><<<g, blk, 0, a.stream>>>(q, k, v, o, a.LSE, a.key_len, a.H, a.Nq, a.Nkv,
-                                                 a.scale, a.causal, num_q_tiles);
+                                                 a.scale, a.causal, num_q_tiles, st);
   else
     fwd_fp32_kernel<128><<<g, blk, 0, a.stream>>>(q, k, v, o, a.LSE, a.key_len, a.H, a.Nq,
-                                                  a.Nkv, a.scale, a.causal, num_q_tiles);
+                                                  a.Nkv, a.scale, a.causal, num_q_tiles, st);
   return cudaGetLastError();
 }
 

@@ -71,19 +71,22 @@ int device_state(DeviceState** out) {
   return OSATTN_OK;
 }
 
-// 3-D bf16 view (d, N, B*H) of a [B, H, N, d] tensor, 64 x 128 boxes,
-// 128-byte swizzle, zero fill outside the tensor.
-int encode_bf16_map(CUtensorMap* map, const void* base, int d, int N, long long BH) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {osattn::kBoxInner, osattn::kBoxRows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+// 4-D view (d, N, H, B) of a tensor with element strides st = {b, h, row}
+// (d contiguous), 64 x 128 boxes, 128-byte swizzle, zero fill outside it.
+int encode_map(CUtensorMap* map, const void* base, int fp16, int d, int N, int H, int B,
+               const long long* st) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2,
+                                 static_cast<cuuint64_t>(st[1]) * 2,
+                                 static_cast<cuuint64_t>(st[0]) * 2};
+  const cuuint32_t box[4] = {osattn::kBoxInner, osattn::kBoxRows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode_tiled(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
@@ -126,6 +129,8 @@ const char* osattn_status_string(int status) {
 
 namespace {
 
+size_t elem_size(int dtype) { return dtype == OSATTN_FP32 ? 4 : 2; }
+
 // Host validation shared by every forward entry point; nothing is enqueued
 // when it fails.
 int validate_fwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
@@ -138,8 +143,28 @@ int validate_fwd(const void* Q, const void* K, const void* V, const void* O, con
       !aligned(LSE, 4) || (key_len && !aligned(key_len, 4)))
     return OSATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return OSATTN_ERR_UNSUPPORTED;
-  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
+  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32 && dtype != OSATTN_FP16)
+    return OSATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return OSATTN_ERR_INVALID_ARG;
+  return OSATTN_OK;
+}
+
+// Element strides {b, h, row}: the caller's, or those of a contiguous
+// [B, H, N, d] tensor when `in` is null.  Every stride must be >= 1 and keep
+// each row 16-byte aligned (a multiple of 16 bytes) and below 2^40 bytes.
+int take_strides(const int64_t* in, int H, int N, int d, int dtype, long long* out) {
+  if (!in) {
+    out[2] = d;
+    out[1] = static_cast<long long>(N) * d;
+    out[0] = static_cast<long long>(H) * N * d;
+    return OSATTN_OK;
+  }
+  const long long es = static_cast<long long>(elem_size(dtype));
+  for (int i = 0; i < 3; ++i) {
+    if (in[i] < 1 || (in[i] * es) % 16 != 0 || in[i] * es >= (1LL << 40))
+      return OSATTN_ERR_INVALID_ARG;
+    out[i] = in[i];
+  }
   return OSATTN_OK;
 }
 
@@ -167,30 +192,62 @@ osattn::FwdArgs make_args(const void* Q, const void* K, const void* V, void* O, 
   return a;
 }
 
-int encode_qkv(const void* Q, const void* K, const void* V, int d, int Nq, int Nkv, long long BH,
-               CUtensorMap* tmQ, CUtensorMap* tmK, CUtensorMap* tmV) {
-  if (encode_bf16_map(tmQ, Q, d, Nq, BH) != OSATTN_OK ||
-      encode_bf16_map(tmK, K, d, Nkv, BH) != OSATTN_OK ||
-      encode_bf16_map(tmV, V, d, Nkv, BH) != OSATTN_OK)
+int encode_qkv(const osattn::FwdArgs& a, CUtensorMap* tmQ, CUtensorMap* tmK, CUtensorMap* tmV) {
+  if (encode_map(tmQ, a.Q, a.fp16, a.d, a.Nq, a.H, a.B, a.q_strides) != OSATTN_OK ||
+      encode_map(tmK, a.K, a.fp16, a.d, a.Nkv, a.H, a.B, a.k_strides) != OSATTN_OK ||
+      encode_map(tmV, a.V, a.fp16, a.d, a.Nkv, a.H, a.B, a.v_strides) != OSATTN_OK)
     return OSATTN_ERR_CUDA;
   return OSATTN_OK;
 }
 
 // Split-KV launch over caller-provided partial buffers: the key-range split
-// of the bf16 kernel, then the combine.  Arguments are already validated.
+// of the tensor-core kernel, then the combine.  Arguments are validated.
 int launch_splitkv(osattn::FwdArgs a, int num_splits, float* o_part, float* lse_part) {
   CUtensorMap tmQ, tmK, tmV;
-  const long long BH = static_cast<long long>(a.B) * a.H;
-  if (encode_qkv(a.Q, a.K, a.V, a.d, a.Nq, a.Nkv, BH, &tmQ, &tmK, &tmV) != OSATTN_OK)
-    return OSATTN_ERR_CUDA;
+  if (encode_qkv(a, &tmQ, &tmK, &tmV) != OSATTN_OK) return OSATTN_ERR_CUDA;
   a.num_splits = num_splits;
   a.o_part = o_part;
   a.lse_part = lse_part;
   if (osattn::launch_fwd_bf16(a, tmQ, tmK, tmV) != cudaSuccess) return OSATTN_ERR_CUDA;
-  if (osattn::launch_splitkv_combine(o_part, lse_part, a.O, a.LSE, BH * a.Nq, a.d, num_splits,
+  const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
+  if (osattn::launch_splitkv_combine(o_part, lse_part, a.O, a.LSE, rows, a.d, num_splits, a.fp16,
                                      a.stream) != cudaSuccess)
     return OSATTN_ERR_CUDA;
   return OSATTN_OK;
+}
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+             int Nq, int Nkv, int d, const int64_t* q_strides, const int64_t* k_strides,
+             const int64_t* v_strides, const int64_t* o_strides, float scale, int causal,
+             const int32_t* key_len, int dtype, void* stream) {
+  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  long long qs[3], ks[3], vs[3], os[3];
+  if (take_strides(q_strides, H, Nq, d, dtype, qs) != OSATTN_OK ||
+      take_strides(k_strides, H, Nkv, d, dtype, ks) != OSATTN_OK ||
+      take_strides(v_strides, H, Nkv, d, dtype, vs) != OSATTN_OK ||
+      take_strides(o_strides, H, Nq, d, dtype, os) != OSATTN_OK)
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  osattn::FwdArgs a = make_args(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, causal, key_len, stream, st);
+  for (int i = 0; i < 3; ++i) {
+    a.q_strides[i] = qs[i];
+    a.k_strides[i] = ks[i];
+    a.v_strides[i] = vs[i];
+    a.o_strides[i] = os[i];
+  }
+  cudaError_t e;
+  if (dtype == OSATTN_FP32) {
+    e = osattn::launch_fwd_fp32(a);
+  } else {
+    a.fp16 = dtype == OSATTN_FP16;
+    CUtensorMap tmQ, tmK, tmV;
+    if (encode_qkv(a, &tmQ, &tmK, &tmV) != OSATTN_OK) return OSATTN_ERR_CUDA;
+    e = osattn::launch_fwd_bf16(a, tmQ, tmK, tmV);
+  }
+  return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -200,23 +257,17 @@ extern "C" {
 int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
                int dtype, void* stream) {
-  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
-  if (rc != OSATTN_OK) return rc;
-  DeviceState* st = nullptr;
-  rc = device_state(&st);
-  if (rc != OSATTN_OK) return rc;
-  osattn::FwdArgs a = make_args(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, causal, key_len, stream, st);
-  cudaError_t e;
-  if (dtype == OSATTN_FP32) {
-    e = osattn::launch_fwd_fp32(a);
-  } else {
-    CUtensorMap tmQ, tmK, tmV;
-    if (encode_qkv(Q, K, V, d, Nq, Nkv, static_cast<long long>(B) * H, &tmQ, &tmK, &tmV) !=
-        OSATTN_OK)
-      return OSATTN_ERR_CUDA;
-    e = osattn::launch_fwd_bf16(a, tmQ, tmK, tmV);
-  }
-  return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+  return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, d, nullptr, nullptr, nullptr, nullptr, scale,
+                  causal, key_len, dtype, stream);
+}
+
+int osattn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                       int H, int Nq, int Nkv, int d, const int64_t* q_strides,
+                       const int64_t* k_strides, const int64_t* v_strides,
+                       const int64_t* o_strides, float scale, int causal,
+                       const int32_t* key_len, int dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, Nq, Nkv, d, q_strides, k_strides, v_strides, o_strides,
+                  scale, causal, key_len, dtype, stream);
 }
 
 size_t osattn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
@@ -231,7 +282,7 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        size_t workspace_bytes, void* stream) {
   int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
   if (rc != OSATTN_OK) return rc;
-  if (dtype != OSATTN_BF16) return OSATTN_ERR_UNSUPPORTED;
+  if (dtype == OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
   if (num_splits < 1 || num_splits > OSATTN_MAX_SPLITS) return OSATTN_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
@@ -240,6 +291,11 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
   rc = device_state(&st);
   if (rc != OSATTN_OK) return rc;
   osattn::FwdArgs a = make_args(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, causal, key_len, stream, st);
+  a.fp16 = dtype == OSATTN_FP16;
+  take_strides(nullptr, H, Nq, d, dtype, a.q_strides);
+  take_strides(nullptr, H, Nkv, d, dtype, a.k_strides);
+  take_strides(nullptr, H, Nkv, d, dtype, a.v_strides);
+  take_strides(nullptr, H, Nq, d, dtype, a.o_strides);
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = o_part + static_cast<size_t>(num_splits) * B * H * Nq * d;
   return launch_splitkv(a, num_splits, o_part, lse_part);
@@ -248,15 +304,16 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
 int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,
                         void* stream) {
   if (!in || !out || rows < 1 || N < 1) return OSATTN_ERR_INVALID_ARG;
-  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
-  const uintptr_t el = dtype == OSATTN_BF16 ? 2 : 4;
+  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32 && dtype != OSATTN_FP16)
+    return OSATTN_ERR_UNSUPPORTED;
+  const uintptr_t el = elem_size(dtype);
   if (!aligned(in, el) || !aligned(out, el) || (lse && !aligned(lse, 4)))
     return OSATTN_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != OSATTN_OK) return rc;
   const cudaError_t e = osattn::launch_softmax_rows(in, out, lse, static_cast<long long>(rows), N,
-                                                    dtype == OSATTN_FP32, st->num_sms,
+                                                    dtype, st->num_sms,
                                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }

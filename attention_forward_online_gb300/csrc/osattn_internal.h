@@ -28,13 +28,18 @@ struct FwdArgs {
   int num_splits = 0;
   float* o_part = nullptr;
   float* lse_part = nullptr;
+  int fp16 = 0;  // 16-bit element type: 0 bf16, 1 fp16
+  // Element strides of the b, h and row axes (the d axis is contiguous).
+  long long q_strides[3] = {0, 0, 0}, k_strides[3] = {0, 0, 0}, v_strides[3] = {0, 0, 0},
+            o_strides[3] = {0, 0, 0};
 };
 
 // fp32 SIMT kernel (fwd_fp32_simt.cu).
 cudaError_t launch_fwd_fp32(const FwdArgs& a);
 
-// bf16 tcgen05 kernel (fwd_bf16_tcgen05.cu).  The tensor maps describe Q, K
-// and V as 3-D bf16 views (d, N, B*H) with 128-byte swizzled 64 x 128 boxes.
+// Tensor-core kernel for 16-bit inputs (fwd_bf16_tcgen05.cu).  The tensor
+// maps describe Q, K and V as 4-D views (d, N, H, B) with the caller's
+// strides and 128-byte swizzled 64 x 128 boxes.
 cudaError_t prepare_fwd_bf16();  // once per device: kernel attributes
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV);
@@ -42,12 +47,13 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
 // Split-KV combine (splitkv_combine.cu): folds the partials of each row with
 // the (m, l) combine and writes O (bf16) and LSE.
 cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* O,
-                                   float* LSE, long long rows, int d, int num_splits,
+                                   float* LSE, long long rows, int d, int num_splits, int fp16,
                                    cudaStream_t stream);
 
-// Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix.
+// Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix;
+// elem: 0 bf16, 1 fp32, 2 fp16 (the public dtype codes).
 cudaError_t launch_softmax_rows(const void* in, void* out, float* lse, long long rows, int N,
-                                int dtype_fp32, int num_sms, cudaStream_t stream);
+                                int elem, int num_sms, cudaStream_t stream);
 
 // Box shape the bf16 kernel expects in its tensor maps.
 constexpr int kBoxInner = 64;   // elements along d (128 bytes)

@@ -107,6 +107,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 4-D tiled load (c0 innermost).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
 // Same, with an L2 cache-policy hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map,
                                                  uint64_t* bar, int c0, int c1, int c2,
@@ -225,13 +236,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
-//   (1 = bf16), 15 A major (0 = K), 16 B major (0 = K, 1 = MN),
+// Instruction descriptor for kind::f16 with fp32 accumulation and A, B both
+// bf16 (ab_fp16 = 0) or both fp16 (ab_fp16 = 1).
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16), 15 A major (0 = K), 16 B major (0 = K, 1 = MN),
 //   17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major, int ab_fp16) {
+  return (1u << 4) | ((ab_fp16 ? 0u : 1u) << 7) | ((ab_fp16 ? 0u : 1u) << 10) |
+         (static_cast<uint32_t>(b_mn_major & 1) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major & 1) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc_f16_f32(M, N, b_mn_major, 0);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
@@ -313,6 +330,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ float fmin3(float a, float b, float c) {
   float r;
   asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

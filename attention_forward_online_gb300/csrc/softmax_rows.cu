@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "osattn_internal.h"
 
@@ -97,6 +98,31 @@ struct Vec<__nv_bfloat16> {
   }
   __device__ static float get(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
   __device__ static void put(__nv_bfloat16* p, long long i, float v) { p[i] = __float2bfloat16_rn(v); }
+};
+template <>
+struct Vec<__half> {
+  static constexpr int N = 8;
+  __device__ static void load(const __half* p, float* v) {
+    const uint4 x = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+  __device__ static void store(__half* p, const float* v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static float get(const __half* p, long long i) { return __half2float(p[i]); }
+  __device__ static void put(__half* p, long long i, float v) { p[i] = __float2half_rn(v); }
 };
 
 // Row held in registers: each thread owns NV 16-byte vectors (32 elements),
@@ -242,8 +268,9 @@ cudaError_t launch_any(const void* in, void* out, float* lse, long long rows, in
 }  // namespace
 
 cudaError_t launch_softmax_rows(const void* in, void* out, float* lse, long long rows, int N,
-                                int dtype_fp32, int num_sms, cudaStream_t stream) {
-  if (dtype_fp32) return launch_any<float>(in, out, lse, rows, N, num_sms, stream);
+                                int elem, int num_sms, cudaStream_t stream) {
+  if (elem == 1) return launch_any<float>(in, out, lse, rows, N, num_sms, stream);
+  if (elem == 2) return launch_any<__half>(in, out, lse, rows, N, num_sms, stream);
   return launch_any<__nv_bfloat16>(in, out, lse, rows, N, num_sms, stream);
 }
 

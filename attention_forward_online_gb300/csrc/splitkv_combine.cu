@@ -14,20 +14,33 @@
 // result up to rounding.
 //
 // One warp per row; each lane owns d/32 consecutive columns (a float4 or
-// float2 per partial), so each partial row is one coalesced 256/512-byte read.
+// float2 per partial), so each partial row is one coalesced 256/512-byte
+// read.  O is written as bf16 or fp16, the type of the inputs.
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "osattn_internal.h"
 
 namespace osattn {
 namespace {
 
-template <int HD>
+template <typename T>
+__device__ __forceinline__ void store2(T* dst, float a, float b);
+template <>
+__device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a, b);
+}
+template <>
+__device__ __forceinline__ void store2<__half>(__half* dst, float a, float b) {
+  *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(a, b);
+}
+
+template <int HD, typename T>
 __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __restrict__ o_part,
                                                               const float* __restrict__ lse_part,
-                                                              __nv_bfloat16* __restrict__ O,
+                                                              T* __restrict__ O,
                                                               float* __restrict__ LSE,
                                                               long long rows, int num_splits) {
   constexpr int CPL = HD / 32;  // columns per lane
@@ -58,27 +71,36 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
     m = M;
   }
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat16* dst = O + row * HD + lane * CPL;
+  T* dst = O + row * HD + lane * CPL;
 #pragma unroll
-  for (int c = 0; c < CPL; c += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + c) = __floats2bfloat162_rn(acc[c] * inv_l, acc[c + 1] * inv_l);
+  for (int c = 0; c < CPL; c += 2) store2<T>(dst + c, acc[c] * inv_l, acc[c + 1] * inv_l);
   if (lane == 0) LSE[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 }  // namespace
 
 cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* O,
-                                   float* LSE, long long rows, int d, int num_splits,
+                                   float* LSE, long long rows, int d, int num_splits, int fp16,
                                    cudaStream_t stream) {
   constexpr int kRowsPerBlock = 8;
   const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(blocks)), b(kRowsPerBlock * 32);
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(O);
-  if (d == 64)
-    splitkv_combine_kernel<64><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows, num_splits);
-  else
-    splitkv_combine_kernel<128><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows, num_splits);
+  if (fp16) {
+    __half* o = static_cast<__half*>(O);
+    if (d == 64)
+      splitkv_combine_kernel<64, __half><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows, num_splits);
+    else
+      splitkv_combine_kernel<128, __half><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows, num_splits);
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(O);
+    if (d == 64)
+      splitkv_combine_kernel<64, __nv_bfloat16><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows,
+                                                                    num_splits);
+    else
+      splitkv_combine_kernel<128, __nv_bfloat16><<<g, b, 0, stream>>>(o_part, lse_part, o, LSE, rows,
+                                                                     num_splits);
+  }
   return cudaGetLastError();
 }
 

@@ -21,10 +21,13 @@ from typing import Optional, Tuple
 import torch
 
 
+TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str            # "bf16" or "fp32"
+    dtype: str            # "bf16", "fp16" or "fp32"
     B: int
     H: int
     Nq: int
@@ -48,7 +51,7 @@ class Workload:
         return f / 2 if self.causal else f
 
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return TORCH_DTYPES[self.dtype]
 
 
 WORKLOADS = {
@@ -88,11 +91,11 @@ class RowWorkload:
     std: float = 3.0
 
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return TORCH_DTYPES[self.dtype]
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == "bf16" else 4
+        return 4 if self.dtype == "fp32" else 2
 
     @property
     def bytes_moved(self) -> int:

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(PKG, "libosattn.so")
 
 BF16 = 0
 FP32 = 1
+FP16 = 2
 OK = 0
 ERR_INVALID_ARG = 1
 ERR_UNSUPPORTED = 2
@@ -26,8 +27,8 @@ ERR_TIMEOUT = 4
 ERR_SCRATCH_LIMIT = 5
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
-EXPORTS = ("osattn_fwd", "osattn_fwd_splitkv", "osattn_splitkv_workspace_bytes",
-           "osattn_fwd_splitkv_noalloc", "osattn_softmax_rows",
+EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
+           "osattn_splitkv_workspace_bytes", "osattn_fwd_splitkv_noalloc", "osattn_softmax_rows",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -56,6 +57,11 @@ def lib():
             L.osattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp, i32, vp]
             L.osattn_fwd.restype = i32
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            L.osattn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                             i64p, i64p, i64p, i64p,
+                                             ctypes.c_float, i32, vp, i32, vp]
+            L.osattn_fwd_strided.restype = i32
             L.osattn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                              ctypes.c_float, i32, vp, i32, i32, vp,
                                              ctypes.c_size_t, vp]
@@ -103,48 +109,90 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nkv, d, scale, causal
                             int(dtype), stream_handle)
 
 
-def fwd(q, k, v, scale: float | None = None, causal: bool = False, key_len=None,
-        out=None, lse=None, stream=None):
-    """O, LSE = attention forward of CUDA tensors q [B,H,Nq,d], k/v [B,H,Nkv,d].
-
-    dtype bf16 or fp32 (all three alike); key_len: None or a CUDA int32
-    tensor [B].  `out` / `lse` may be given preallocated (contiguous, the
-    right shape and dtype).  Enqueued on `stream` (default: torch's current
-    stream); raises OsattnError if the library rejects the call."""
+def _dtype_code(t) -> int:
     import torch
 
-    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v must all be bf16 or all fp32")
+    codes = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
+    if t.dtype not in codes:
+        raise TypeError("q, k, v must all be bf16, all fp16 or all fp32")
+    return codes[t.dtype]
+
+
+def _shapes(q, k, v):
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, H, N, d]")
     B, H, Nq, d = q.shape
     Nkv = k.shape[2]
     if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
         raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
     for t in (q, k, v):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
+        if not t.is_cuda:
+            raise ValueError("q, k, v must be CUDA tensors")
+    return B, H, Nq, Nkv, d
+
+
+def _key_len_ptr(key_len, B):
+    import torch
+
+    if key_len is None:
+        return None, None
+    if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+        raise ValueError("key_len must be a CUDA int32 tensor with B entries")
+    key_len = key_len.contiguous()
+    return key_len, key_len.data_ptr()
+
+
+def _bhn_strides(t):
+    """(b, h, row) element strides of a [B, H, N, d] view whose d axis is
+    contiguous, as a ctypes int64[3]."""
+    if t.stride(3) != 1:
+        raise ValueError("the last (d) axis must have stride 1")
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def fwd(q, k, v, scale: float | None = None, causal: bool = False, key_len=None,
+        out=None, lse=None, stream=None):
+    """O, LSE = attention forward of CUDA tensors q [B,H,Nq,d], k/v [B,H,Nkv,d].
+
+    dtype bf16, fp16 or fp32 (all three alike).  q, k, v and `out` may be any
+    views whose last axis is contiguous (e.g. transposes of [B, N, H, d]);
+    contiguous tensors go through osattn_fwd, others through
+    osattn_fwd_strided with their strides.  key_len: None or a CUDA int32
+    tensor [B].  `out` (q's shape and dtype) and `lse` (contiguous fp32
+    [B, H, Nq]) may be given preallocated.  Enqueued on `stream` (default:
+    torch's current stream); raises OsattnError if the library rejects the
+    call."""
+    import torch
+
+    B, H, Nq, Nkv, d = _shapes(q, k, v)
+    dtype = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must match q")
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_cuda:
+        raise ValueError("out must be a CUDA tensor matching q")
     if tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be fp32 [B, H, Nq]")
-    kl_ptr = None
-    if key_len is not None:
-        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
-            raise ValueError("key_len must be a CUDA int32 tensor with B entries")
-        key_len = key_len.contiguous()
-        kl_ptr = key_len.data_ptr()
-    dtype = BF16 if q.dtype == torch.bfloat16 else FP32
-    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                 B, H, Nq, Nkv, d, scale, causal, kl_ptr, dtype, _stream_handle(stream))
+    kl, kl_ptr = _key_len_ptr(key_len, B)
+    if all(t.is_contiguous() for t in (q, k, v, out)):
+        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                     B, H, Nq, Nkv, d, scale, causal, kl_ptr, dtype, _stream_handle(stream))
+        what = "osattn_fwd"
+    else:
+        qs, ks, vs, os_ = (_bhn_strides(t) for t in (q, k, v, out))
+        st = lib().osattn_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), B, H, Nq, Nkv, d, qs, ks, vs, os_,
+                                      float(scale), int(bool(causal)), kl_ptr, dtype,
+                                      _stream_handle(stream))
+        what = "osattn_fwd_strided"
+    del kl
     if st != OK:
-        raise OsattnError(st, "osattn_fwd")
+        raise OsattnError(st, what)
     return out, lse
 
 
@@ -157,25 +205,17 @@ def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) ->
 
 
 def _check_qkv(q, k, v):
-    import torch
-
-    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v must all be bf16 or all fp32")
-    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
-        raise ValueError("q, k, v must be [B, H, N, d]")
-    B, H, Nq, d = q.shape
-    Nkv = k.shape[2]
-    if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
-        raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    B, H, Nq, Nkv, d = _shapes(q, k, v)
+    _dtype_code(q)
     for t in (q, k, v):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
     return B, H, Nq, Nkv, d
 
 
 def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bool = False,
                 key_len=None, out=None, lse=None, workspace=None, stream=None):
-    """Split-KV attention forward (bf16): same result as fwd(), the key axis cut
+    """Split-KV attention forward (bf16 or fp16): same result as fwd(), the key axis cut
     into num_splits ranges merged by the (m, l) combine.  `workspace` may be a
     preallocated CUDA uint8 tensor of at least splitkv_workspace_bytes(...)
     bytes; otherwise torch allocates one."""
@@ -189,13 +229,8 @@ def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bo
     need = splitkv_workspace_bytes(B, H, Nq, d, max(int(num_splits), 1))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    kl_ptr = None
-    if key_len is not None:
-        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
-            raise ValueError("key_len must be a CUDA int32 tensor with B entries")
-        key_len = key_len.contiguous()
-        kl_ptr = key_len.data_ptr()
-    dtype = BF16 if q.dtype == torch.bfloat16 else FP32
+    key_len, kl_ptr = _key_len_ptr(key_len, B)
+    dtype = _dtype_code(q)
     st = lib().osattn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   lse.data_ptr(), B, H, Nq, Nkv, d, float(scale),
                                   int(bool(causal)), kl_ptr, dtype, int(num_splits),
@@ -207,19 +242,20 @@ def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bo
 
 
 def softmax_rows(x, out=None, lse=None, want_lse: bool = True, stream=None):
-    """Row softmax of a contiguous CUDA [rows, N] bf16/fp32 tensor (online (m, l)
+    """Row softmax of a contiguous CUDA [rows, N] bf16/fp16/fp32 tensor (online (m, l)
     normaliser).  Returns (y, lse or None); `out` may be `x` (in place)."""
     import torch
 
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA [rows, N] tensor")
-    if x.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("x must be bf16 or fp32")
+    codes = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
+    if x.dtype not in codes:
+        raise TypeError("x must be bf16, fp16 or fp32")
     rows, N = x.shape
     out = torch.empty_like(x) if out is None else out
     if want_lse and lse is None:
         lse = torch.empty(rows, dtype=torch.float32, device=x.device)
-    dtype = BF16 if x.dtype == torch.bfloat16 else FP32
+    dtype = codes[x.dtype]
     st = lib().osattn_softmax_rows(x.data_ptr(), out.data_ptr(),
                                    None if lse is None else lse.data_ptr(), rows, N, dtype,
                                    _stream_handle(stream))

@@ -31,6 +31,7 @@ extern "C" {
 /* Element types of Q, K, V and O (LSE is always fp32). */
 #define OSATTN_BF16 0 /* bfloat16; runs on the tcgen05 tensor-core kernel */
 #define OSATTN_FP32 1 /* float32; runs on the SIMT kernel (full fp32 FMA) */
+#define OSATTN_FP16 2 /* IEEE float16; runs on the tcgen05 tensor-core kernel */
 
 /* Status codes. */
 #define OSATTN_OK 0
@@ -68,7 +69,8 @@ extern "C" {
  *   key_len  device int32 [B] or NULL; keys j >= key_len[b] are masked
  *            (values are clamped to [0, Nkv]; NULL means Nkv for every b).
  *            Combined with `causal` by logical AND.
- *   dtype    OSATTN_BF16 or OSATTN_FP32
+ *   dtype    OSATTN_BF16, OSATTN_FP16 (tensor cores, fp32 accumulation,
+ *            P rounded to the input type before P.V) or OSATTN_FP32 (SIMT)
  *   stream   cudaStream_t to enqueue on (NULL: the legacy default stream)
  *
  * Layout and alignment: Q, K, V and O must be 16-byte aligned; LSE and
@@ -91,6 +93,30 @@ int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                int B, int H, int Nq, int Nkv, int d, float scale, int causal,
                const int32_t* key_len, int dtype, void* stream);
 
+/*
+ * osattn_fwd_strided - osattn_fwd on tensors with arbitrary strides, e.g.
+ * the [B, N, H, d] layout a fused QKV projection leaves behind, without a
+ * transposing copy.  Same computation, masking, results and errors as
+ * osattn_fwd.
+ *
+ *   q_strides, k_strides, v_strides, o_strides
+ *            host int64[3] each, or NULL: element strides of the B, H and
+ *            sequence axes of Q, K, V and O (the d axis always has stride 1).
+ *            NULL means the contiguous [B, H, N, d] layout, so osattn_fwd is
+ *            this call with four NULLs.  Each stride must be >= 1, a multiple
+ *            of 16 bytes (8 elements for bf16/fp16, 4 for fp32) and below
+ *            2^40 bytes; otherwise OSATTN_ERR_INVALID_ARG.  Strides are read
+ *            during the call only.  Views may interleave (Q, K and V slices
+ *            of one packed tensor); O must not alias any input, and distinct
+ *            (b, h, i) of O must not share memory.
+ *   LSE      always [B, H, Nq] contiguous fp32.
+ */
+int osattn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       int B, int H, int Nq, int Nkv, int d, const int64_t* q_strides,
+                       const int64_t* k_strides, const int64_t* v_strides,
+                       const int64_t* o_strides, float scale, int causal,
+                       const int32_t* key_len, int dtype, void* stream);
+
 /* Largest num_splits osattn_fwd_splitkv accepts. */
 #define OSATTN_MAX_SPLITS 128
 
@@ -111,10 +137,11 @@ size_t osattn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_split
  * partial O_s = O / l_s (fp32) and lse_s = m_s + ln l_s; a second kernel
  * folds the partials of every row with the guarded (m, l) combine of [Ch6]
  * §6.4.1 - the two-stage reduction [Ch6] §6.7.1 describes for a row split
- * across blocks - and writes O (bf16) and LSE.  A key range with no visible
+ * across blocks - and writes O and LSE.  A key range with no visible
  * key contributes the (-inf, 0) identity.
  *
- *   dtype            OSATTN_BF16 only (OSATTN_FP32 -> OSATTN_ERR_UNSUPPORTED)
+ *   dtype            OSATTN_BF16 or OSATTN_FP16 (OSATTN_FP32 -> OSATTN_ERR_UNSUPPORTED);
+ *                    O is written in that type
  *   num_splits       1 .. OSATTN_MAX_SPLITS (else OSATTN_ERR_INVALID_ARG); ranges are
  *                    equal cuts of each 256-row query block's 128-key tiles, so
  *                    splits beyond the tile count receive empty ranges
@@ -173,7 +200,8 @@ int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void
  * once; longer rows are read twice.  -inf entries act as the additive mask
  * of [Ch6] §6.7.3; a row of only -inf gives y = 0 and LSE = -inf (no NaN).
  *
- *   in, out  device, [rows, N] contiguous, element type `dtype` (bf16 or fp32);
+ *   in, out  device, [rows, N] contiguous, element type `dtype` (bf16, fp16
+ *            or fp32);
  *            element-aligned; in == out (in place) is allowed
  *   lse      device fp32 [rows], or NULL to skip it
  *   rows, N  >= 1

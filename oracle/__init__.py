@@ -29,6 +29,7 @@ _lib = None
 DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 DTYPE_FP64 = 2
+DTYPE_FP16 = 3
 
 
 def build(force: bool = False) -> str:
@@ -134,12 +135,16 @@ def _as_raw(t):
         t = t.detach().to("cpu").contiguous()
         if t.dtype == torch.bfloat16:
             return t.view(torch.int16).numpy(), DTYPE_BF16
+        if t.dtype == torch.float16:
+            return t.view(torch.int16).numpy(), DTYPE_FP16
         if t.dtype == torch.float32:
             return t.numpy(), DTYPE_FP32
         if t.dtype == torch.float64:
             return t.numpy(), DTYPE_FP64
         raise TypeError(f"unsupported dtype {t.dtype}")
     a = np.ascontiguousarray(t)
+    if a.dtype == np.float16:
+        return a.view(np.int16), DTYPE_FP16
     if a.dtype == np.float32:
         return a, DTYPE_FP32
     if a.dtype == np.float64:
@@ -151,10 +156,11 @@ def attention_fwd(Q, K, V, scale: float, causal: bool = False, key_len=None,
                   rows=None, nthreads: int = 0):
     """Attention forward by the definition (three-pass safe softmax per row).
 
-    Q: [B,H,Nq,d]; K, V: [B,H,Nkv,d] (torch bf16/fp32/fp64 or numpy
-    fp32/fp64, all of one dtype).  key_len: None or B ints.  rows: None for
-    every row (returns O [B,H,Nq,d], LSE [B,H,Nq]) or a list of flat row
-    indices (b*H+h)*Nq+i (returns O [n,d], LSE [n]).  Results are fp64."""
+    Q: [B,H,Nq,d]; K, V: [B,H,Nkv,d] (torch bf16/fp16/fp32/fp64 or numpy
+    fp16/fp32/fp64, all of one dtype; any strides: the values are read).
+    key_len: None or B ints.  rows: None for every row (returns O
+    [B,H,Nq,d], LSE [B,H,Nq]) or a list of flat row indices (b*H+h)*Nq+i
+    (returns O [n,d], LSE [n]).  Results are fp64."""
     q, dt = _as_raw(Q)
     k, dk = _as_raw(K)
     v, dv = _as_raw(V)
@@ -188,8 +194,8 @@ def attention_fwd(Q, K, V, scale: float, causal: bool = False, key_len=None,
 
 
 def softmax_rows(X, nthreads: int = 0):
-    """Row softmax of a [rows, N] tensor (torch bf16/fp32/fp64 or numpy
-    fp32/fp64) by the three-pass safe softmax, row by row (ch. 6 §6.2); also
+    """Row softmax of a [rows, N] tensor (torch bf16/fp16/fp32/fp64 or numpy
+    fp16/fp32/fp64) by the three-pass safe softmax, row by row (ch. 6 §6.2); also
     returns the row LSE (§6.5).  All -inf rows give y = 0, LSE = -inf."""
     x, dt = _as_raw(X)
     if x.ndim != 2:

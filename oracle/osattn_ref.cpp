@@ -51,8 +51,25 @@ namespace {
 const double kNegInf = -std::numeric_limits<double>::infinity();
 
 // Element formats the oracle can read.  bf16 is the top half of an IEEE
-// binary32, so widening is a shift; every bf16/fp32 value is exact in double.
-enum RefDtype { REF_BF16 = 0, REF_FP32 = 1, REF_FP64 = 2 };
+// binary32, so widening is a shift; fp16 is IEEE binary16, decoded from its
+// fields below; every bf16/fp16/fp32 value is exact in double.
+enum RefDtype { REF_BF16 = 0, REF_FP32 = 1, REF_FP64 = 2, REF_FP16 = 3 };
+
+// IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+// bits.  Exponent 0 holds zero and the subnormals f * 2^-24; exponent 31
+// holds infinity (f = 0) and NaN.
+inline double decode_binary16(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 0x1f, f = h & 0x3ff;
+  double mag;
+  if (e == 0)
+    mag = std::ldexp(static_cast<double>(f), -24);
+  else if (e == 31)
+    mag = f == 0 ? std::numeric_limits<double>::infinity()
+                 : std::numeric_limits<double>::quiet_NaN();
+  else
+    mag = std::ldexp(static_cast<double>(1024 + f), e - 25);
+  return sign ? -mag : mag;
+}
 
 inline double load_elem(const void* base, int dtype, int64_t idx) {
   if (dtype == REF_BF16) {
@@ -62,6 +79,11 @@ inline double load_elem(const void* base, int dtype, int64_t idx) {
     float f;
     std::memcpy(&f, &u, 4);
     return static_cast<double>(f);
+  }
+  if (dtype == REF_FP16) {
+    uint16_t h;
+    std::memcpy(&h, static_cast<const uint16_t*>(base) + idx, 2);
+    return decode_binary16(h);
   }
   if (dtype == REF_FP32) {
     float f;
@@ -136,7 +158,7 @@ void attention_row(const AttnProblem& p, int64_t flat_row, double* o_row,
 int check_problem(const AttnProblem& p) {
   if (!p.Q || !p.K || !p.V) return 1;
   if (p.B < 1 || p.H < 1 || p.Nq < 1 || p.Nkv < 1 || p.d < 1) return 1;
-  if (p.dtype < REF_BF16 || p.dtype > REF_FP64) return 1;
+  if (p.dtype < REF_BF16 || p.dtype > REF_FP16) return 1;
   return 0;
 }
 
@@ -238,11 +260,11 @@ double osattn_ref_lse(double m, double l) {
 // Row softmax of a [rows, N] matrix by the three-pass safe softmax of
 // [Ch6] §6.2, row by row: y = e^{x - m} / l with m = max x, l = sum e^{x - m},
 // and lse = m + log l ([Ch6] §6.5).  A row of only -inf (all masked) has no
-// defined softmax; it yields y = 0 and lse = -inf.  x is bf16 bits, fp32 or
-// fp64 (dtype 0/1/2); y and lse are double; lse may be null.
+// defined softmax; it yields y = 0 and lse = -inf.  x is bf16 bits, fp32,
+// fp64 or fp16 bits (dtype 0/1/2/3); y and lse are double; lse may be null.
 int osattn_ref_softmax_rows(const void* x, int dtype, int64_t rows, int N, double* y,
                             double* lse, int nthreads) {
-  if (!x || !y || rows < 1 || N < 1 || dtype < REF_BF16 || dtype > REF_FP64) return 1;
+  if (!x || !y || rows < 1 || N < 1 || dtype < REF_BF16 || dtype > REF_FP16) return 1;
   parallel_rows(rows, nthreads, [&](int64_t r) {
     const int64_t base = r * N;
     double m = kNegInf;
@@ -259,7 +281,7 @@ int osattn_ref_softmax_rows(const void* x, int dtype, int64_t rows, int N, doubl
 
 // Attention forward by the definition in the file header.
 //   Q: [B,H,Nq,d], K/V: [B,H,Nkv,d], contiguous, element format `dtype`
-//   (0 bf16 bits, 1 fp32, 2 fp64).  key_len: host int32 [B] or null.
+//   (0 bf16 bits, 1 fp32, 2 fp64, 3 fp16 bits).  key_len: host int32 [B] or null.
 //   rows == null: every row; O receives [B,H,Nq,d], LSE [B,H,Nq].
 //   rows != null: only the nrows flat row indices (b*H+h)*Nq+i listed there;
 //   O receives [nrows,d] and LSE [nrows], in list order.

@@ -143,3 +143,53 @@ def test_softmax_rows_host_validation(L):
     assert f(P, P + 2, None, 4, 8, osattn.FP32, nul) == osattn.ERR_INVALID_ARG
     assert f(P, P, P + 2, 4, 8, osattn.FP32, nul) == osattn.ERR_INVALID_ARG
     assert f(P, P, None, 4, 8, 9, nul) == osattn.ERR_UNSUPPORTED
+
+
+def call_strided(strides=(None, None, None, None), **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=8, Nkv=8, d=64, scale=0.125, causal=0,
+             key_len=None, dtype=osattn.BF16)
+    a.update(kw)
+    arrs = [None if s is None else (ctypes.c_int64 * 3)(*s) for s in strides]
+    return osattn.lib().osattn_fwd_strided(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                           a["H"], a["Nq"], a["Nkv"], a["d"], *arrs, a["scale"],
+                                           a["causal"], a["key_len"], a["dtype"],
+                                           ctypes.c_void_p(None))
+
+
+BNHD = (8 * 2 * 64, 64, 2 * 64)  # [B, N, H, d] storage seen as [B, H, N, d]
+
+
+@pytest.mark.parametrize("strides,dtype", [
+    ((BNHD, BNHD, BNHD, (0, 64, 128)), osattn.BF16),          # zero stride
+    ((BNHD, (-64, 64, 128), BNHD, BNHD), osattn.BF16),         # negative stride
+    (((1024, 64, 132), BNHD, BNHD, BNHD), osattn.BF16),        # row 264 B: not 16-B multiple
+    ((BNHD, BNHD, (1024, 68, 128), BNHD), osattn.FP16),        # head 136 B
+    ((BNHD, BNHD, BNHD, (1024, 64, 130)), osattn.FP32),        # fp32 row 520 B
+    ((BNHD, BNHD, BNHD, (1 << 40, 64, 128)), osattn.BF16),     # >= 2^40 bytes
+])
+def test_strided_host_validation(L, strides, dtype):
+    assert call_strided(strides, dtype=dtype) == osattn.ERR_INVALID_ARG
+
+
+def test_strided_shares_osattn_fwd_checks(L):
+    assert call_strided(q=None) == osattn.ERR_INVALID_ARG
+    assert call_strided(d=96) == osattn.ERR_UNSUPPORTED
+    assert call_strided(dtype=3) == osattn.ERR_UNSUPPORTED
+    assert call_strided(o=P + 8) == osattn.ERR_INVALID_ARG
+
+
+def test_fp16_dtype_passes_host_validation_like_bf16(L):
+    # Same rejections for fp16 as for bf16 (the first failing check decides).
+    assert call(dtype=osattn.FP16, d=96) == osattn.ERR_UNSUPPORTED
+    assert call(dtype=osattn.FP16, q=P + 8) == osattn.ERR_INVALID_ARG
+    assert call_split(dtype=osattn.FP16, splits=0) == osattn.ERR_INVALID_ARG
+    f = L.osattn_softmax_rows
+    assert f(P + 1, P, None, 4, 8, osattn.FP16, ctypes.c_void_p(None)) == osattn.ERR_INVALID_ARG
+
+
+def test_binding_rejects_non_unit_inner_stride(L):
+    import torch
+
+    q = torch.zeros(1, 1, 64, 4, dtype=torch.bfloat16).transpose(2, 3)  # d axis strided
+    with pytest.raises(ValueError):
+        osattn._bhn_strides(q)

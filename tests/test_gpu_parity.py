@@ -34,8 +34,11 @@ def run_gpu(q, k, v, scale, causal, key_len):
     return O.double().cpu().numpy(), L.double().cpu().numpy()
 
 
+KIND = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
+
+
 def kind_of(t):
-    return "bf16" if t.dtype == torch.bfloat16 else "fp32"
+    return KIND[t.dtype]
 
 
 EDGE = [
@@ -57,7 +60,7 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else "") + f"kl{c[6]}")
 def test_edge_shapes_full_parity(case, dtype):
     B, H, Nq, Nkv, d, causal, kl, q_std = case
@@ -68,7 +71,7 @@ def test_edge_shapes_full_parity(case, dtype):
     check(O, L, Oref, Lref, kind_of(q))
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
 def test_worked_example_through_kernel(dtype):
     # Logits (1, 5, 3) for one query (chapter 6 §6.3.2), V = identity on the
     # first three columns, so O[0:3] is the printed probability vector.

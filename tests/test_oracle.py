@@ -212,7 +212,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES)
-@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16, torch.float16])
 def test_attention_matches_library_route(ref, case, dtype):
     B, H, Nq, Nkv, d, causal, kl = case
     g = torch.Generator().manual_seed(11)
@@ -237,6 +237,21 @@ def test_attention_single_key_is_that_value(ref):
     O, L = ref.attention_fwd(q, k, v, scale=0.3)
     np.testing.assert_allclose(O, np.broadcast_to(v, O.shape), atol=1e-15)
     np.testing.assert_allclose(L, 0.3 * np.einsum("bhid,bhd->bhi", q, k[:, :, 0]), atol=1e-14)
+
+
+def test_fp16_decoding_every_finite_bit_pattern(ref):
+    # With one key the softmax weight is exactly 1, so O = V: the oracle's
+    # IEEE binary16 decoder must agree with numpy's on all 63488 finite
+    # patterns (zeros, subnormals, normals, both signs).
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    h = bits.view(np.float16)
+    h = h[np.isfinite(h)]
+    assert h.size == 63488
+    v = torch.from_numpy(h.copy()).reshape(1, h.size // 64, 1, 64)
+    q = torch.zeros_like(v)
+    O, L = ref.attention_fwd(q, q, v, scale=1.0)
+    assert np.array_equal(O.reshape(-1), h.astype(np.float64))
+    assert np.all(L == 0.0)
 
 
 def test_attention_zero_query_averages_visible_values(ref):
@@ -351,7 +366,7 @@ def test_oracle_rejects_bad_arguments(ref):
 
 
 # ---------------------------------------------------------------- batched row softmax
-@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16, torch.float16])
 def test_softmax_rows_matches_scipy_and_worked_example(ref, golden, dtype):
     g = torch.Generator().manual_seed(21)
     X = (torch.randn(37, 301, generator=g, dtype=torch.float64) * 5).to(dtype)

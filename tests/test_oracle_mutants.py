@@ -31,6 +31,10 @@ MUTANTS = {
     "online_no_rescale": ("l = l * std::exp(m - m_new) + std::exp(x[t] - m_new);",
                           "l = l + std::exp(x[t] - m_new);"),
     "lse_log2": ("return m + std::log(l);\n}", "return m + std::log2(l);\n}"),
+    "fp16_exponent_bias": ("mag = std::ldexp(static_cast<double>(1024 + f), e - 25);",
+                           "mag = std::ldexp(static_cast<double>(1024 + f), e - 24);"),
+    "fp16_subnormal_scale": ("mag = std::ldexp(static_cast<double>(f), -24);",
+                             "mag = std::ldexp(static_cast<double>(1024 + f), -25);"),
 }
 
 
