@@ -25,11 +25,15 @@
 //               new row max, publish alpha, P_t = bf16(2^(x - m)) written
 //               over S_t in tensor memory, l = l * alpha + rowsum(P).
 //               At the end, the epilogue O / l and LSE for the tile.
-//   warps 8-11  correction: once PV_t of the previous K/V tile is done,
-//               multiply O_t by alpha in tensor memory - only warps holding
+//   warps 8-11  correction: once S_t of this K/V tile (and so PV_t of the
+//               previous one) is done, multiply O_t by alpha in tensor memory - only warps holding
 //               a row whose max moved do it.  Off the softmax's path.
 //   warp 12     TMA producer: Q0, Q1 once, then K_0, V_0, K_1, V_1, ... into
-//               a STAGES-deep ring.
+//               a STAGES-deep ring.  MMA iteration j reads V_{j-1} and K_j,
+//               so one barrier per iteration covers both loads and one
+//               commit per iteration frees both stages: the MMA thread
+//               (whose issue of one MMA takes most of the MMA's 64 cycles)
+//               spends as little as possible on barrier checks.
 //   warp 13     allocates tensor memory; one thread issues the MMAs in the
 //               order S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... so the
 //               tensor core computes one tile's S while the other tile's
@@ -69,7 +73,6 @@ enum : uint32_t {
   kSiteMmaP = 4,
   kSiteSoftS = 5,
   kSiteCorrAlpha = 6,
-  kSiteCorrO = 7,
   kSiteEpiO = 8
 };
 
@@ -78,18 +81,22 @@ struct Cfg {
   static constexpr int kTileBytes = BN * HD * 2;  // one K or V tile
   static constexpr int kQBytes = BM * HD * 2;     // one query tile
   static constexpr int kStages = HD == 128 ? 5 : 12;
+  // Ring of per-iteration K/V barriers.  The producer arms iteration i after
+  // iteration i - kStages/2 - 1 has released its stages, so the MMA has
+  // passed iteration i - kIters by then (kIters > kStages/2 + 1).
+  static constexpr int kIters = HD == 128 ? 4 : 8;
   static constexpr int kTileRegion = kQTiles * kQBytes + kStages * kTileBytes;
   static constexpr uint32_t kOCol0 = 256;
 };
 
 struct __align__(8) Bars {
   uint64_t q_full[kQTiles];
-  uint64_t kv_full[16];
-  uint64_t kv_empty[16];
+  uint64_t kv_full[8];    // [i % kIters]: V_{i-1} and K_i, which MMA iteration i reads, have landed
+  uint64_t kv_empty[8];   // [i % kIters]: the MMAs of iteration i are done (their stages are free)
   uint64_t s_full[kQTiles];      // MMA -> softmax: S_t ready
   uint64_t alpha_full[kQTiles];  // softmax -> correction: alpha published (128 arrivals)
   uint64_t p_full[kQTiles];      // softmax + correction -> MMA: P_t written, O_t rescaled (256)
-  uint64_t o_full[kQTiles];      // MMA -> correction / epilogue: PV_t done
+  uint64_t o_full[kQTiles];      // MMA -> epilogue: the tile's last PV done
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -263,7 +270,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
 
   // ---------------------------------------------------------------- epilogue
   if (ok && n_t > 0) {
-    ok = mbar_wait(&bars->o_full[t], static_cast<uint32_t>(n_t - 1) & 1u, wc, kSiteEpiO);
+    ok = mbar_wait(&bars->o_full[t], 0u, wc, kSiteEpiO);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) tc_fence_after_sync();
   }
@@ -336,15 +343,16 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
 
 // ------------------------------------------------------------------ correction
 // Multiplies O_t by alpha in tensor memory once PV_t of the previous K/V
-// tile has completed, for warps holding a row whose max moved; then signals
+// tile has completed (implied by alpha_full, see below), for warps holding a row whose max moved; then signals
 // the MMA warp (together with the softmax) that PV_t may run.
 template <int HD>
 __device__ __forceinline__ void correction_tile(Bars* bars, uint32_t lane_base, int row, int t,
                                                 int j, bool& ok, WaitCtl wc) {
   using C = Cfg<HD>;
+  // alpha_full(j) follows s_full(j): S_t(j) is complete, and so is PV_t(j-1),
+  // issued before it (the MMA pipe runs in issue order and a commit tracks
+  // every earlier MMA of the thread), so O_t may be rescaled now.
   ok = mbar_wait(&bars->alpha_full[t], static_cast<uint32_t>(j) & 1u, wc, kSiteCorrAlpha);
-  if (ok && j > 0)
-    ok = mbar_wait(&bars->o_full[t], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteCorrO);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return;
   const float alpha = bars->alpha[t][row];
@@ -408,24 +416,38 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
     for (int cb = 0; cb < HD / 64; ++cb)
       tma_load_4d(sQ + C::kQBytes + cb * BM * 128, tmQ, &bars->q_full[1], cb * 64, q0 + BM, h, b);
   }
-  const int total = 2 * max(n0, n1);  // K_0, V_0, K_1, V_1, ...
-  int u = 0;
+  // Load u goes to stage u % kStages: K_j for u = 2j, V_j for u = 2j + 1.
+  // MMA iteration i reads V_{i-1} and K_i (loads 2i - 1 and 2i), so both
+  // signal kv_full[i % kIters], armed once with their combined size, and
+  // load u waits only for the iteration that last read its stage.
+  const int n = max(n0, n1);
+  const int total = 2 * n;
+  int u = 0, armed = 0;
   for (; u < total; ++u) {
     const int s = u % C::kStages;
-    const uint32_t round = static_cast<uint32_t>(u / C::kStages);
-    if (!mbar_wait(&bars->kv_empty[s], (round & 1u) ^ 1u, wc, kSiteProdEmpty)) break;
-    mbar_arrive_expect_tx(&bars->kv_full[s], C::kTileBytes);
+    if (u >= C::kStages) {
+      const int r = (u - C::kStages + 1) >> 1;  // iteration that read load u - kStages
+      if (!mbar_wait(&bars->kv_empty[r % C::kIters], static_cast<uint32_t>(r / C::kIters) & 1u, wc,
+                     kSiteProdEmpty))
+        break;
+    }
+    const int i = (u + 1) >> 1;  // iteration that reads load u
+    uint64_t* full = &bars->kv_full[i % C::kIters];
+    if (u == 0 || (u & 1)) {  // first load of iteration i
+      mbar_arrive_expect_tx(full, ((i < n) ? C::kTileBytes : 0) + ((i >= 1) ? C::kTileBytes : 0));
+      armed = i + 1;
+    }
     uint8_t* dst = sKV + s * C::kTileBytes;
     const CUtensorMap* map = (u & 1) ? tmV : tmK;
 #pragma unroll
     for (int cb = 0; cb < HD / 64; ++cb)
-      tma_load_4d(dst + cb * BN * 128, map, &bars->kv_full[s], cb * 64, (sb + (u >> 1)) * BN, h, b);
+      tma_load_4d(dst + cb * BN * 128, map, full, cb * 64, (sb + (u >> 1)) * BN, h, b);
   }
   // Let every load this thread issued land before the CTA can exit.
   if (n0 > 0) drain_wait(&bars->q_full[0], 0, wc.limit_ns);
   if (n1 > 0) drain_wait(&bars->q_full[1], 0, wc.limit_ns);
-  for (int v = (u > C::kStages ? u - C::kStages : 0); v < u; ++v)
-    drain_wait(&bars->kv_full[v % C::kStages], static_cast<uint32_t>(v / C::kStages) & 1u,
+  for (int i = (armed > C::kIters ? armed - C::kIters : 0); i < armed; ++i)
+    drain_wait(&bars->kv_full[i % C::kIters], static_cast<uint32_t>(i / C::kIters) & 1u,
                wc.limit_ns);
 }
 
@@ -470,18 +492,11 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
   bool ok = true;
 
   for (int j = 0; ok && j <= n; ++j) {
-    // K_j sits at load slot 2j, V_{j-1} at 2j - 1.
-    uint32_t vs = 0, ks = 0;
-    if (j > 0) {
-      const int u = 2 * j - 1;
-      vs = static_cast<uint32_t>(u % C::kStages);
-      ok = mbar_wait(&bars->kv_full[vs], static_cast<uint32_t>(u / C::kStages) & 1u, wc, kSiteMmaKV);
-    }
-    if (ok && j < n) {
-      const int u = 2 * j;
-      ks = static_cast<uint32_t>(u % C::kStages);
-      ok = mbar_wait(&bars->kv_full[ks], static_cast<uint32_t>(u / C::kStages) & 1u, wc, kSiteMmaKV);
-    }
+    // K_j sits at load slot 2j, V_{j-1} at 2j - 1; one barrier covers both.
+    const uint32_t vs = j > 0 ? static_cast<uint32_t>((2 * j - 1) % C::kStages) : 0u;
+    const uint32_t ks = static_cast<uint32_t>((2 * j) % C::kStages);
+    ok = mbar_wait(&bars->kv_full[j % C::kIters], static_cast<uint32_t>(j / C::kIters) & 1u, wc,
+                   kSiteMmaKV);
     if (ok && j == 0) {
       if (n0 > 0) ok = mbar_wait(&bars->q_full[0], 0, wc, kSiteMmaQ);
       if (ok && n1 > 0) ok = mbar_wait(&bars->q_full[1], 0, wc, kSiteMmaQ);
@@ -494,7 +509,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       if (!ok) break;
       tc_fence_after_sync();
       issue_pv<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
-      mma_commit(&bars->o_full[0]);
+      if (j == n0) mma_commit(&bars->o_full[0]);
     }
     if (j < n0) {
       issue_s<HD, kF16>(s_col0, q_desc0, k_desc + ks * kStageStep);
@@ -506,14 +521,13 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       if (!ok) break;
       tc_fence_after_sync();
       issue_pv<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
-      mma_commit(&bars->o_full[1]);
+      if (j == n1) mma_commit(&bars->o_full[1]);
     }
     if (j < n1) {
       issue_s<HD, kF16>(s_col1, q_desc1, k_desc + ks * kStageStep);
       mma_commit(&bars->s_full[1]);
     }
-    if (j > 0) mma_commit(&bars->kv_empty[vs]);
-    if (j < n) mma_commit(&bars->kv_empty[ks]);
+    mma_commit(&bars->kv_empty[j % C::kIters]);
   }
   // Every MMA this thread issued must complete before tensor memory is freed.
   mma_commit(&bars->mma_drain);
@@ -571,9 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[t], 256);
       mbar_init(&bars->o_full[t], 1);
     }
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int i = 0; i < C::kIters; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
     }
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
