@@ -458,10 +458,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 template <int HD, bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   constexpr uint32_t idS = idesc_f16_f32(BM, BN, 0, kF16);  // K-major A and B
+  mma_ss_k<0>(d_tmem, a_desc, b_desc, idS);
 #pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idS, kk > 0 ? 1u : 0u);
+  for (int kk = 1; kk < HD / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
+    mma_ss_k<1>(d_tmem, sdesc_add(a_desc, off), sdesc_add(b_desc, off), idS);
   }
 }
 
@@ -471,10 +472,11 @@ template <int HD, bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idPV = idesc_f16_f32(BM, HD, 1, kF16);  // B (V) is MN-major
+  mma_bf16_ts(o_tmem, p_tmem, v_desc, idPV, accumulate ? 1u : 0u);
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk)
-    mma_bf16_ts(o_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idPV,
-                (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 1; kk < BN / 16; ++kk)
+    mma_ts_k<1>(o_tmem, p_tmem + kk * 8, sdesc_add(v_desc, static_cast<uint32_t>((kk * 2048) >> 4)),
+                idPV);
 }
 
 template <int HD, bool kF16>

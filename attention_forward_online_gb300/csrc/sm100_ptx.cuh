@@ -273,6 +273,44 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Adds an offset (16-byte units) to the start-address field of a shared-memory
+// descriptor.  The field (bits 0-13) holds a shared-memory address >> 4 and
+// cannot carry out, so one 32-bit add on the low word does it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t off16) {
+  uint64_t r;
+  asm("{\n\t.reg .b32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tadd.u32 lo, lo, %2;\n\tmov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r)
+      : "l"(d), "r"(off16));
+  return r;
+}
+
+// mma_bf16_ss / mma_bf16_ts with a compile-time accumulate flag: the
+// predicate folds away, so each MMA costs the issuing thread one instruction
+// less.  The MMA thread shares its sub-partition's issue slots with two
+// softmax warps, so its instruction count per MMA sets how fast it can feed
+// the tensor core.
+template <int kAcc>
+__device__ __forceinline__ void mma_ss_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+
+template <int kAcc>
+__device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op this thread issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
