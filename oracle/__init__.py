@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the attention forward pass (test infrastructure only).
+"""fp64 CPU oracle for the attention forward pass and its gradients (test
+infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
 baseline use this package.  The product library never imports it, and it
@@ -64,6 +65,10 @@ def _load():
             ctypes.c_double, ctypes.c_int, vp, vp, ctypes.c_int64, ctypes.c_int]
         lib.osattn_ref_softmax_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                                 dp, dp, ctypes.c_int]
+        lib.osattn_ref_attention_bwd.argtypes = [
+            vp, vp, vp, vp, ctypes.c_int, dp, dp, dp,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int, vp, ctypes.c_int]
         lib.osattn_ref_attention_blocked.argtypes = [
             vp, vp, vp, ctypes.c_int, dp, dp,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -191,6 +196,39 @@ def attention_fwd(Q, K, V, scale: float, causal: bool = False, key_len=None,
     if rc:
         raise ValueError("invalid arguments to the oracle")
     return O, L
+
+
+def attention_bwd(Q, K, V, dO, scale: float, causal: bool = False, key_len=None,
+                  nthreads: int = 0):
+    """Gradients (dQ, dK, dV) of the attention forward for an upstream
+    gradient dO shaped like O, by the chain rule on the definition (see
+    osattn_ref.cpp).  Q, dO: [B,H,Nq,d]; K, V: [B,H,Nkv,d], one dtype (as for
+    attention_fwd).  Results are fp64."""
+    q, dt = _as_raw(Q)
+    k, dk = _as_raw(K)
+    v, dv = _as_raw(V)
+    g, dg = _as_raw(dO)
+    if not (dt == dk == dv == dg):
+        raise TypeError("Q, K, V, dO must share one dtype")
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if k.shape != (B, H, Nkv, d) or v.shape != (B, H, Nkv, d) or g.shape != q.shape:
+        raise ValueError("shape mismatch")
+    kl = None
+    if key_len is not None:
+        kl = np.ascontiguousarray(np.asarray(key_len, dtype=np.int32).reshape(-1))
+        if kl.size != B:
+            raise ValueError("key_len must have B entries")
+    dQ = np.empty((B, H, Nq, d))
+    dK = np.empty((B, H, Nkv, d))
+    dV = np.empty((B, H, Nkv, d))
+    rc = _load().osattn_ref_attention_bwd(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, dt, _dptr(dQ), _dptr(dK),
+        _dptr(dV), B, H, Nq, Nkv, d, float(scale), int(bool(causal)),
+        None if kl is None else kl.ctypes.data, int(nthreads))
+    if rc:
+        raise ValueError("invalid arguments to the oracle")
+    return dQ, dK, dV
 
 
 def softmax_rows(X, nthreads: int = 0):

@@ -1,4 +1,5 @@
-// osattn_ref.cpp - fp64 CPU oracle for the attention forward pass.
+// osattn_ref.cpp - fp64 CPU oracle for the attention forward pass and its
+// gradients.
 //
 // TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 // benchmark's CPU-baseline leg load this library.  The product (libosattn)
@@ -371,6 +372,78 @@ int osattn_ref_attention_blocked(const void* Q, const void* K, const void* V, in
     } else {
       for (int c = 0; c < d; ++c) o[c] = 0.0;
       LSE[flat] = kNegInf;
+    }
+  });
+  return 0;
+}
+
+// Gradients of the forward pass above for an upstream gradient dO (one
+// array shaped like O, element format `dtype`).  [Ch6] §6.5 keeps only LSE
+// per row from the forward pass so that the backward pass can rebuild the
+// probabilities, and [XXQK] §5.2 (last paragraph) recomputes S there; the
+// derivatives are the chain rule applied to the definition in this file's
+// header (nothing else is assumed):
+//   P_ij  = exp(s_ij - LSE_i) for j in J_i, else 0
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = <dO_i, V_j>
+//   D_i   = sum_j P_ij dP_ij                 (equals <dO_i, O_i>)
+//   dS_ij = P_ij (dP_ij - D_i)               (softmax Jacobian)
+//   dQ_i  = scale * sum_j dS_ij K_j
+//   dK_j  = scale * sum_i dS_ij Q_i
+// A row with J empty contributes nothing.  dQ [B,H,Nq,d], dK and dV
+// [B,H,Nkv,d], all double.  One thread per (b, h).
+// Returns 0, or 1 for an invalid argument (nothing written).
+int osattn_ref_attention_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                             int dtype, double* dQ, double* dK, double* dV, int B, int H, int Nq,
+                             int Nkv, int d, double scale, int causal, const int32_t* key_len,
+                             int nthreads) {
+  AttnProblem p{Q, K, V, dtype, B, H, Nq, Nkv, d, scale, causal, key_len};
+  if (check_problem(p) || !dO || !dQ || !dK || !dV) return 1;
+  parallel_rows(static_cast<int64_t>(B) * H, nthreads, [&](int64_t bh) {
+    const int b = static_cast<int>(bh / H);
+    const int64_t qbase = bh * static_cast<int64_t>(Nq) * d;
+    const int64_t kbase = bh * static_cast<int64_t>(Nkv) * d;
+    for (int64_t e = 0; e < static_cast<int64_t>(Nkv) * d; ++e) {
+      dK[kbase + e] = 0.0;
+      dV[kbase + e] = 0.0;
+    }
+    std::vector<double> s(Nkv), pr(Nkv), dp(Nkv);
+    for (int i = 0; i < Nq; ++i) {
+      double* dq = dQ + qbase + static_cast<int64_t>(i) * d;
+      for (int c = 0; c < d; ++c) dq[c] = 0.0;
+      int jend = visible_keys(p, b);
+      if (causal) jend = std::min(jend, i + 1);
+      if (jend <= 0) continue;
+      const int64_t qoff = qbase + static_cast<int64_t>(i) * d;
+      for (int j = 0; j < jend; ++j) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k)
+          acc += load_elem(Q, dtype, qoff + k) * load_elem(K, dtype, kbase + static_cast<int64_t>(j) * d + k);
+        s[j] = scale * acc;
+      }
+      double m = kNegInf;
+      for (int j = 0; j < jend; ++j) m = std::max(m, s[j]);
+      double l = 0.0;
+      for (int j = 0; j < jend; ++j) l += std::exp(s[j] - m);
+      const double lse = m + std::log(l);
+      double D = 0.0;
+      for (int j = 0; j < jend; ++j) {
+        pr[j] = std::exp(s[j] - lse);
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+          acc += load_elem(dO, dtype, qoff + c) * load_elem(V, dtype, kbase + static_cast<int64_t>(j) * d + c);
+        dp[j] = acc;
+        D += pr[j] * dp[j];
+      }
+      for (int j = 0; j < jend; ++j) {
+        const double ds = pr[j] * (dp[j] - D);
+        const int64_t koff = kbase + static_cast<int64_t>(j) * d;
+        for (int c = 0; c < d; ++c) {
+          dq[c] += scale * ds * load_elem(K, dtype, koff + c);
+          dK[koff + c] += scale * ds * load_elem(Q, dtype, qoff + c);
+          dV[koff + c] += pr[j] * load_elem(dO, dtype, qoff + c);
+        }
+      }
     }
   });
   return 0;

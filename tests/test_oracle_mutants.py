@@ -2,8 +2,9 @@
 
 Each mutant is a one-line change to a copy of ``oracle/osattn_ref.cpp`` that
 a plausible bug would make (dropped term, wrong sign or index, transposed
-operand, off-by-one mask).  The oracle pins in ``test_oracle.py`` run against
-the copy in a child process (a bad index may crash it), and must not pass.
+operand, off-by-one mask).  The oracle pins in ``test_oracle.py`` and
+``test_oracle_bwd.py`` run against the copy in a child process (a bad index
+may crash it), and must not pass.
 CPU only; the real oracle is never modified.
 """
 import os
@@ -35,6 +36,14 @@ MUTANTS = {
                            "mag = std::ldexp(static_cast<double>(1024 + f), e - 24);"),
     "fp16_subnormal_scale": ("mag = std::ldexp(static_cast<double>(f), -24);",
                              "mag = std::ldexp(static_cast<double>(1024 + f), -25);"),
+    "bwd_drops_row_term": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * dp[j];"),
+    "bwd_sign": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * (D - dp[j]);"),
+    "bwd_dk_without_scale": ("dK[koff + c] += scale * ds * load_elem(Q, dtype, qoff + c);",
+                             "dK[koff + c] += ds * load_elem(Q, dtype, qoff + c);"),
+    "bwd_dv_wrong_operand": ("dV[koff + c] += pr[j] * load_elem(dO, dtype, qoff + c);",
+                             "dV[koff + c] += pr[j] * load_elem(Q, dtype, qoff + c);"),
+    "bwd_dq_transposed_key": ("dq[c] += scale * ds * load_elem(K, dtype, koff + c);",
+                              "dq[c] += scale * ds * load_elem(K, dtype, kbase + static_cast<int64_t>(c % Nkv) * d + j % d);"),
 }
 
 
@@ -51,6 +60,6 @@ def test_planted_mistake_is_caught(tmp_path, name):
     env = dict(os.environ, OSATTN_ORACLE_DIR=str(dst))
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-         os.path.join(ROOT, "tests", "test_oracle.py")],
+         os.path.join(ROOT, "tests", "test_oracle.py"), os.path.join(ROOT, "tests", "test_oracle_bwd.py")],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
