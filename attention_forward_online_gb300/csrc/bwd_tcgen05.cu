@@ -1,0 +1,635 @@
+// bwd_tcgen05.cu - gradients of the attention forward pass (dQ, dK, dV) on
+// the Blackwell tensor cores (tcgen05 MMAs, accumulators in tensor memory,
+// operands staged by TMA).  Built for sm_103a.
+//
+// The forward pass keeps one number per query row, LSE = m + ln l (chapter 6
+// "Softmax 与 Online Softmax" of the hand-written FlashAttention v2 book,
+// §6.5), and the backward pass rebuilds the scores from Q and K instead of
+// storing them (m.xxqk.cn/news/563265 §5.2, last paragraph).  With
+// P_ij = e^{s_ij - LSE_i} on the visible keys the chain rule gives
+//   D_i   = <dO_i, O_i>                 (= sum_j P_ij dP_ij)
+//   dP_ij = <dO_i, V_j>,  dS_ij = P_ij (dP_ij - D_i)
+//   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j.
+//
+// Three launches on one stream:
+//   bwd_rowdot_kernel  D = rowsum(dO * O) in fp32 (HBM-bound, one warp a row).
+//   bwd_dkdv_kernel    one CTA per 128-key tile of a (b, h): K and V stay in
+//                      shared memory while the query tiles that can see
+//                      those keys stream through a TMA ring.  Per query tile:
+//                        S^T  = K Q^T   and  dP^T = V dO^T   (tensor memory)
+//                        P^T, dS^T in 16-bit over the first halves of both
+//                        dV += P^T dO   and  dK += dS^T Q     (A from tensor memory)
+//   bwd_dq_kernel      one CTA per 128-row query tile: Q and dO stay, the
+//                      visible K/V tiles stream.  Per key tile:
+//                        S = Q K^T  and  dP = dO V^T;  dS in 16-bit over S
+//                        dQ += dS K                            (A from tensor memory)
+// S and dP are computed twice (once per kernel) so that no kernel needs
+// atomics: each output element is written once, by one CTA.
+//
+// CTA layout (192 threads): warps 0-3 elementwise (one tile row per thread,
+// tensor-memory lane = row), warp 4 producer (TMA; its lanes stage LSE and
+// D of the dK/dV kernel's query tiles), warp 5 allocates tensor memory and
+// one of its threads issues the MMAs.  Every wait is bounded as in the
+// forward kernel: a wait past the limit records OSATTN_ERR_TIMEOUT, the CTA
+// drains its own copies and MMAs, frees tensor memory and returns.
+//
+// Tensor memory (512 columns): [0, 128) S or S^T (then P / dS packed in its
+// first 64 columns), [128, 256) dP or dP^T (dS^T packed in its first 64),
+// [256, 256 + d) dV or dQ, [256 + d, 256 + 2d) dK.
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "osattn_internal.h"
+#include "sm100_ptx.cuh"
+#include "tc_attn_mma.cuh"
+
+namespace osattn {
+namespace {
+
+constexpr int kT = 128;            // rows of every tile (keys or queries)
+constexpr int kBwdThreads = 192;   // warps 0-3 elementwise, 4 producer, 5 MMA
+constexpr int kProdWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Give-up sites recorded in the status word's second slot.
+enum : uint32_t { kSiteBwdLoad = 21, kSiteBwdMma = 22, kSiteBwdElem = 23, kSiteBwdEpi = 24 };
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int kTileBytes = kT * HD * 2;       // one 128-row tile
+  static constexpr int kStages = HD == 128 ? 2 : 4;    // ring stages, two tiles each
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRegion = 2 * kTileBytes + kStages * kStageBytes;  // fixed pair + ring
+  static constexpr uint32_t kColAcc0 = 256;            // dV or dQ
+  static constexpr uint32_t kColAcc1 = 256 + HD;       // dK
+};
+
+struct __align__(8) BwdBars {
+  uint64_t fixed_full;            // the tile pair loaded once (K, V or Q, dO)
+  uint64_t full[4], empty[4];     // ring stages
+  uint64_t sd_full;               // MMA -> elementwise: the two score tiles are ready
+  uint64_t p_full;                // elementwise -> MMA: the 16-bit operands are written (128)
+  uint64_t acc_full;              // MMA -> epilogue: the last accumulation is done
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  float lse2[4][kT];              // dK/dV kernel, per stage: LSE * log2(e) of the tile's queries
+  float dsum[4][kT];              //   and their D (+inf and 0 for rows past Nq)
+};
+
+template <int HD>
+constexpr int bwd_smem_bytes() {
+  return BwdCfg<HD>::kRegion + static_cast<int>(sizeof(BwdBars)) + 1024;
+}
+
+struct BwdParams {
+  uint16_t* dQ;
+  uint16_t* dK;
+  uint16_t* dV;
+  const float* LSE;
+  const float* D;
+  const int32_t* key_len;
+  int H, Nq, Nkv;
+  int num_tiles;     // 128-row tiles per (b, h): of keys (dK/dV) or queries (dQ)
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  unsigned int* status;
+  uint64_t wait_limit_ns;
+};
+
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kF16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__device__ __forceinline__ int clamp_key_len(const int32_t* key_len, int b, int Nkv) {
+  return key_len ? min(max(key_len[b], 0), Nkv) : Nkv;
+}
+
+// Writes one 128-row tile row of `cols` fp32 tensor-memory columns starting
+// at col0, times `mul`, as 16-bit values to dst (or zeros when has_acc is
+// false).  The loads are warp-wide; only the stores depend on `store`.
+template <int HD, bool kF16>
+__device__ __forceinline__ void write_row(uint16_t* dst, uint32_t taddr, bool has_acc, bool store,
+                                          float mul) {
+#pragma unroll
+  for (int ch = 0; ch < HD / 32; ++ch) {
+    uint32_t r[32];
+    if (has_acc) {
+      tmem_ld_32x32b_x32(taddr + ch * 32, r);
+      tmem_ld_wait();
+      reg_fence32(r);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pk[e] = pack2<kF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+    if (store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ D = rowsum(dO * O)
+template <typename T>
+__device__ __forceinline__ float2 load2(const T* p);
+template <>
+__device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <>
+__device__ __forceinline__ float2 load2<__half>(const __half* p) {
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O,
+                                                         const T* __restrict__ dO,
+                                                         float* __restrict__ D, long long rows,
+                                                         int d) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < rows; row += warps) {
+    const T* o = O + row * d;
+    const T* g = dO + row * d;
+    float acc = 0.f;
+    for (int c = 2 * lane; c < d; c += 64) {
+      const float2 a = load2<T>(o + c), b = load2<T>(g + c);
+      acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) D[row] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int HD, bool kF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const BwdParams p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTileBytes;
+  uint8_t* ring = smem + 2 * C::kTileBytes;  // stage s: Q_i at +0, dO_i at +kTileBytes
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kRegion);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bh = blockIdx.x / p.num_tiles;
+  const int kt = blockIdx.x % p.num_tiles;  // key tile 0 first: it meets the most query tiles
+  const int b = bh / p.H, h = bh % p.H;
+  const int k0 = kt * kT;
+  const int kv_len = clamp_key_len(p.key_len, b, p.Nkv);
+  const int nqt = (p.Nq + kT - 1) / kT;
+  // Query tiles that can see this key tile: causal ones start at the tile
+  // holding query k0 (key j is visible to query i iff j <= i).
+  const int it0 = p.causal ? k0 / kT : 0;
+  const int n_it = k0 < kv_len ? max(0, nqt - it0) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fixed_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->sd_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->mma_drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort_flag, p.status, p.status + 1, p.wait_limit_ns};
+
+  if (warp == kProdWarp) {
+    // ---------------------------------------------------------------- producer
+    int issued = 0;
+    if (n_it > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_load_4d(sK + cb * kT * 128, &tmK, &bars->fixed_full, cb * 64, k0, h, b);
+          tma_load_4d(sV + cb * kT * 128, &tmV, &bars->fixed_full, cb * 64, k0, h, b);
+        }
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % C::kStages;
+        bool ok = true;
+        if (it >= C::kStages)
+          ok = mbar_wait(&bars->empty[s], static_cast<uint32_t>(it / C::kStages - 1) & 1u, wc,
+                         kSiteBwdLoad);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int q0 = (it0 + it) * kT;
+        const long long rowbase = static_cast<long long>(bh) * p.Nq;
+#pragma unroll
+        for (int r = 0; r < kT / 32; ++r) {
+          const int qq = lane + 32 * r, q = q0 + qq;
+          float l2 = INFINITY, dd = 0.f;
+          if (q < p.Nq) {
+            const float L = p.LSE[rowbase + q];
+            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+            dd = p.D[rowbase + q];
+          }
+          bars->lse2[s][qq] = l2;
+          bars->dsum[s][qq] = dd;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          uint8_t* st = ring + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[s], 2 * C::kTileBytes);
+#pragma unroll
+          for (int cb = 0; cb < HD / 64; ++cb) {
+            tma_load_4d(st + cb * kT * 128, &tmQ, &bars->full[s], cb * 64, q0, h, b);
+            tma_load_4d(st + C::kTileBytes + cb * kT * 128, &tmdO, &bars->full[s], cb * 64, q0, h, b);
+          }
+        }
+        issued = it + 1;
+      }
+      // Let every load of this CTA land before it can exit.
+      if (lane == 0) {
+        drain(&bars->fixed_full, 0, wc.limit_ns);
+        for (int it = (issued > C::kStages ? issued - C::kStages : 0); it < issued; ++it)
+          drain(&bars->full[it % C::kStages], static_cast<uint32_t>(it / C::kStages) & 1u,
+                wc.limit_ns);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_it > 0) {
+      const uint64_t kA = sdesc_sw128(smem_u32(sK), 16, 1024);  // K-major A
+      const uint64_t vA = sdesc_sw128(smem_u32(sV), 16, 1024);
+      bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::kStages;
+        ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t sq = smem_u32(ring + s * C::kStageBytes), sdo = sq + C::kTileBytes;
+        mma_abt_128<HD, kF16>(tmem, kA, sdesc_sw128(sq, 16, 1024));         // S^T = K Q^T
+        mma_abt_128<HD, kF16>(tmem + 128, vA, sdesc_sw128(sdo, 16, 1024));  // dP^T = V dO^T
+        mma_commit(&bars->sd_full);
+        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // dV += P^T dO and dK += dS^T Q: B read MN-major from the same tiles
+        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sdo, kT * 128, 1024), it > 0);
+        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc1, tmem + 128, sdesc_sw128(sq, kT * 128, 1024),
+                                 it > 0);
+        mma_commit(&bars->empty[s]);
+      }
+      if (ok) mma_commit(&bars->acc_full);
+      // Every MMA this thread issued must complete before tensor memory is freed.
+      mma_commit(&bars->mma_drain);
+      drain(&bars->mma_drain, 0, wc.limit_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- elementwise
+    const int row = warp * 32 + lane;  // key row of the tile = tensor-memory lane
+    const int kabs = k0 + row;
+    const bool row_live = kabs < kv_len;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % C::kStages;
+      ok = mbar_wait(&bars->sd_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
+      // LSE and D of this query tile were staged with the stage's loads.
+      if (ok) ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int q0 = (it0 + it) * kT;
+      const float* l2 = bars->lse2[s];
+      const float* dd = bars->dsum[s];
+#pragma unroll 1
+      for (int ch = 0; ch < kT / 32; ++ch) {
+        uint32_t sv[32], dv[32];
+        tmem_ld_32x32b_x32(lane_base + ch * 32, sv);
+        tmem_ld_32x32b_x32(lane_base + 128 + ch * 32, dv);
+        tmem_ld_wait();
+        reg_fence32(sv);
+        reg_fence32(dv);
+        uint32_t pk[16], gk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pr[2], gr[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qq = ch * 32 + 2 * e + u;
+            const bool vis = row_live && (!p.causal || kabs <= q0 + qq);
+            const float x = fmaf(__uint_as_float(sv[2 * e + u]), c, -l2[qq]);
+            pr[u] = vis ? ex2_approx(x) : 0.f;
+            gr[u] = pr[u] * (__uint_as_float(dv[2 * e + u]) - dd[qq]);
+          }
+          pk[e] = pack2<kF16>(pr[0], pr[1]);
+          gk[e] = pack2<kF16>(gr[0], gr[1]);
+        }
+        tmem_st_32x32b_x16(lane_base + ch * 16, pk);
+        tmem_st_32x32b_x16(lane_base + 128 + ch * 16, gk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full);
+    }
+    // epilogue: dV = sum P^T dO, dK = scale * sum dS^T Q
+    bool has_acc = false;
+    if (ok && n_it > 0) {
+      ok = mbar_wait(&bars->acc_full, 0, wc, kSiteBwdEpi);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after_sync();
+      has_acc = ok;
+    }
+    if (ok) {
+      const bool store = kabs < p.Nkv;
+      const long long off = (static_cast<long long>(bh) * p.Nkv + kabs) * HD;
+      write_row<HD, kF16>(p.dV + off, lane_base + C::kColAcc0, has_acc, store, 1.f);
+      write_row<HD, kF16>(p.dK + off, lane_base + C::kColAcc1, has_acc, store, p.scale);
+    }
+  }
+
+  __syncwarp();
+  tmem_st_wait();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int HD, bool kF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = smem + C::kTileBytes;
+  uint8_t* ring = smem + 2 * C::kTileBytes;  // stage s: K_j at +0, V_j at +kTileBytes
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kRegion);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int bh = blockIdx.x / p.num_tiles;
+  int qt = blockIdx.x % p.num_tiles;
+  if (p.causal) qt = p.num_tiles - 1 - qt;  // the longest key loops first
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * kT;
+  const int kv_len = clamp_key_len(p.key_len, b, p.Nkv);
+  int kv_end = kv_len;
+  if (p.causal) kv_end = min(kv_end, q0 + kT);
+  const int n_kt = q0 < p.Nq ? (kv_end + kT - 1) / kT : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fixed_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->sd_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->mma_drain, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort_flag, p.status, p.status + 1, p.wait_limit_ns};
+
+  if (warp == kProdWarp) {
+    if (lane == 0 && n_kt > 0) {
+      mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < HD / 64; ++cb) {
+        tma_load_4d(sQ + cb * kT * 128, &tmQ, &bars->fixed_full, cb * 64, q0, h, b);
+        tma_load_4d(sdO + cb * kT * 128, &tmdO, &bars->fixed_full, cb * 64, q0, h, b);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages &&
+            !mbar_wait(&bars->empty[s], static_cast<uint32_t>(j / C::kStages - 1) & 1u, wc,
+                       kSiteBwdLoad))
+          break;
+        uint8_t* st = ring + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&bars->full[s], 2 * C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb) {
+          tma_load_4d(st + cb * kT * 128, &tmK, &bars->full[s], cb * 64, j * kT, h, b);
+          tma_load_4d(st + C::kTileBytes + cb * kT * 128, &tmV, &bars->full[s], cb * 64, j * kT, h, b);
+        }
+        issued = j + 1;
+      }
+      drain(&bars->fixed_full, 0, wc.limit_ns);
+      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
+        drain(&bars->full[j % C::kStages], static_cast<uint32_t>(j / C::kStages) & 1u, wc.limit_ns);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n_kt > 0) {
+      const uint64_t qA = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dA = sdesc_sw128(smem_u32(sdO), 16, 1024);
+      bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j % C::kStages;
+        ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(j / C::kStages) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t sk = smem_u32(ring + s * C::kStageBytes), sv = sk + C::kTileBytes;
+        mma_abt_128<HD, kF16>(tmem, qA, sdesc_sw128(sk, 16, 1024));        // S = Q K^T
+        mma_abt_128<HD, kF16>(tmem + 128, dA, sdesc_sw128(sv, 16, 1024));  // dP = dO V^T
+        mma_commit(&bars->sd_full);
+        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // dQ += dS K: K read MN-major from the same tile
+        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sk, kT * 128, 1024), j > 0);
+        mma_commit(&bars->empty[s]);
+      }
+      if (ok) mma_commit(&bars->acc_full);
+      mma_commit(&bars->mma_drain);
+      drain(&bars->mma_drain, 0, wc.limit_ns);
+    }
+  } else {
+    const int row = warp * 32 + lane;  // query row of the tile = tensor-memory lane
+    const int q = q0 + row;
+    const bool row_live = q < p.Nq;
+    const long long rix = static_cast<long long>(bh) * p.Nq + q;
+    float l2 = INFINITY, Dq = 0.f;
+    if (row_live && n_kt > 0) {
+      const float L = p.LSE[rix];
+      l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
+      Dq = p.D[rix];
+    }
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      ok = mbar_wait(&bars->sd_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int kb = j * kT;
+#pragma unroll 1
+      for (int ch = 0; ch < kT / 32; ++ch) {
+        uint32_t sv[32], dv[32];
+        tmem_ld_32x32b_x32(lane_base + ch * 32, sv);
+        tmem_ld_32x32b_x32(lane_base + 128 + ch * 32, dv);
+        tmem_ld_wait();
+        reg_fence32(sv);
+        reg_fence32(dv);
+        uint32_t gk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float gr[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int k = kb + ch * 32 + 2 * e + u;
+            const bool vis = k < kv_len && (!p.causal || k <= q);
+            const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), c, -l2)) : 0.f;
+            gr[u] = pr * (__uint_as_float(dv[2 * e + u]) - Dq);
+          }
+          gk[e] = pack2<kF16>(gr[0], gr[1]);
+        }
+        tmem_st_32x32b_x16(lane_base + ch * 16, gk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full);
+    }
+    bool has_acc = false;
+    if (ok && n_kt > 0) {
+      ok = mbar_wait(&bars->acc_full, 0, wc, kSiteBwdEpi);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after_sync();
+      has_acc = ok;
+    }
+    if (ok) write_row<HD, kF16>(p.dQ + rix * HD, lane_base + C::kColAcc0, has_acc, row_live, p.scale);
+  }
+
+  __syncwarp();
+  tmem_st_wait();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+template <int HD, bool kF16>
+cudaError_t set_bwd_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<HD, kF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_smem_bytes<HD>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(bwd_dq_kernel<HD, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bwd_smem_bytes<HD>());
+}
+
+template <int HD, bool kF16>
+cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensorMap& tmQ,
+                         const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO) {
+  const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
+  const long long want = static_cast<long long>(a.num_sms) * 16;
+  const int rgrid = static_cast<int>((rows + 7) / 8 < want ? (rows + 7) / 8 : want);
+  using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
+  bwd_rowdot_kernel<T><<<rgrid, 256, 0, a.stream>>>(static_cast<const T*>(a.O),
+                                                    static_cast<const T*>(a.dO), a.D, rows, a.d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  BwdParams pk = base;
+  pk.num_tiles = (a.Nkv + kT - 1) / kT;
+  const long long gk = static_cast<long long>(pk.num_tiles) * a.B * a.H;
+  BwdParams pq = base;
+  pq.num_tiles = (a.Nq + kT - 1) / kT;
+  const long long gq = static_cast<long long>(pq.num_tiles) * a.B * a.H;
+  if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
+  bwd_dkdv_kernel<HD, kF16><<<static_cast<unsigned>(gk), kBwdThreads, bwd_smem_bytes<HD>(), a.stream>>>(
+      tmQ, tmK, tmV, tmdO, pk);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<HD, kF16><<<static_cast<unsigned>(gq), kBwdThreads, bwd_smem_bytes<HD>(), a.stream>>>(
+      tmQ, tmK, tmV, tmdO, pq);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prepare_bwd() {
+  cudaError_t e;
+  if ((e = set_bwd_attrs<64, false>()) != cudaSuccess) return e;
+  if ((e = set_bwd_attrs<128, false>()) != cudaSuccess) return e;
+  if ((e = set_bwd_attrs<64, true>()) != cudaSuccess) return e;
+  return set_bwd_attrs<128, true>();
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, const CUtensorMap& tmdO) {
+  BwdParams p;
+  p.dQ = static_cast<uint16_t*>(a.dQ);
+  p.dK = static_cast<uint16_t*>(a.dK);
+  p.dV = static_cast<uint16_t*>(a.dV);
+  p.LSE = a.LSE;
+  p.D = a.D;
+  p.key_len = a.key_len;
+  p.H = a.H;
+  p.Nq = a.Nq;
+  p.Nkv = a.Nkv;
+  p.num_tiles = 0;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.causal = a.causal;
+  p.status = a.status;
+  p.wait_limit_ns = a.wait_limit_ns;
+  if (a.d == 64)
+    return a.fp16 ? launch_bwd_t<64, true>(a, p, tmQ, tmK, tmV, tmdO)
+                  : launch_bwd_t<64, false>(a, p, tmQ, tmK, tmV, tmdO);
+  return a.fp16 ? launch_bwd_t<128, true>(a, p, tmQ, tmK, tmV, tmdO)
+                : launch_bwd_t<128, false>(a, p, tmQ, tmK, tmV, tmdO);
+}
+
+}  // namespace osattn

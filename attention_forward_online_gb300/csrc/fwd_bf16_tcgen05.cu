@@ -53,6 +53,7 @@
 
 #include "osattn_internal.h"
 #include "sm100_ptx.cuh"
+#include "tc_attn_mma.cuh"
 
 namespace osattn {
 namespace {
@@ -452,32 +453,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// S_t = Q_t K^T: 128 x 128 fp32 into tensor-memory columns [t*128, t*128+128).
-// a_desc / b_desc address the first 16-element K slice; later slices move 32
-// bytes within a 128-byte swizzle row, or to the next 64-column block.
-template <int HD, bool kF16>
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
-  constexpr uint32_t idS = idesc_f16_f32(BM, BN, 0, kF16);  // K-major A and B
-  mma_ss_k<0>(d_tmem, a_desc, b_desc, idS);
-#pragma unroll
-  for (int kk = 1; kk < HD / 16; ++kk) {
-    const uint32_t off = static_cast<uint32_t>(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
-    mma_ss_k<1>(d_tmem, sdesc_add(a_desc, off), sdesc_add(b_desc, off), idS);
-  }
-}
-
-// O_t (+)= P_t V: P from tensor memory (bf16 pairs over S_t), V MN-major in
-// shared memory; 16 keys per step = two 8-row swizzle atoms (2 KB).
-template <int HD, bool kF16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                         bool accumulate) {
-  constexpr uint32_t idPV = idesc_f16_f32(BM, HD, 1, kF16);  // B (V) is MN-major
-  mma_bf16_ts(o_tmem, p_tmem, v_desc, idPV, accumulate ? 1u : 0u);
-#pragma unroll
-  for (int kk = 1; kk < BN / 16; ++kk)
-    mma_ts_k<1>(o_tmem, p_tmem + kk * 8, sdesc_add(v_desc, static_cast<uint32_t>((kk * 2048) >> 4)),
-                idPV);
-}
+// S_t = Q_t K^T (128 x 128 fp32 into tensor-memory columns [t*128, t*128+128))
+// is mma_abt_128; O_t (+)= P_t V, with P from tensor memory (bf16 pairs over
+// S_t) and V read MN-major from shared memory, is mma_tmem_a_128.
 
 template <int HD, bool kF16>
 __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ, uint8_t* sKV,
@@ -510,11 +488,11 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       ok = mbar_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
       if (!ok) break;
       tc_fence_after_sync();
-      issue_pv<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
+      mma_tmem_a_128<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
       if (j == n0) mma_commit(&bars->o_full[0]);
     }
     if (j < n0) {
-      issue_s<HD, kF16>(s_col0, q_desc0, k_desc + ks * kStageStep);
+      mma_abt_128<HD, kF16>(s_col0, q_desc0, k_desc + ks * kStageStep);
       mma_commit(&bars->s_full[0]);
     }
     // tile 1: PV1(j-1), then S1(j)
@@ -522,11 +500,11 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       ok = mbar_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
       if (!ok) break;
       tc_fence_after_sync();
-      issue_pv<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
+      mma_tmem_a_128<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
       if (j == n1) mma_commit(&bars->o_full[1]);
     }
     if (j < n1) {
-      issue_s<HD, kF16>(s_col1, q_desc1, k_desc + ks * kStageStep);
+      mma_abt_128<HD, kF16>(s_col1, q_desc1, k_desc + ks * kStageStep);
       mma_commit(&bars->s_full[1]);
     }
     mma_commit(&bars->kv_empty[j % C::kIters]);

@@ -56,6 +56,7 @@ int device_state(DeviceState** out) {
         cudaSuccess)
       return OSATTN_ERR_CUDA;
     if (osattn::prepare_fwd_bf16() != cudaSuccess) return OSATTN_ERR_CUDA;
+    if (osattn::prepare_bwd() != cudaSuccess) return OSATTN_ERR_CUDA;
     if (!g_encode_tiled) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -299,6 +300,63 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = o_part + static_cast<size_t>(num_splits) * B * H * Nq * d;
   return launch_splitkv(a, num_splits, o_part, lse_part);
+}
+
+size_t osattn_bwd_workspace_bytes(int B, int H, int Nq) {
+  if (B < 1 || H < 1 || Nq < 1) return 0;
+  return static_cast<size_t>(B) * H * Nq * sizeof(float);
+}
+
+int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+               const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv,
+               int d, float scale, int causal, const int32_t* key_len, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (!dO || !dQ || !dK || !dV || !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) ||
+      !aligned(dV, 16))
+    return OSATTN_ERR_INVALID_ARG;
+  if (dtype == OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < osattn_bwd_workspace_bytes(B, H, Nq))
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != OSATTN_OK) return rc;
+  osattn::BwdArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.dO = dO;
+  a.LSE = LSE;
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.D = static_cast<float*>(workspace);
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nkv = Nkv;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.key_len = key_len;
+  a.fp16 = dtype == OSATTN_FP16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = st->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.num_sms = st->num_sms;
+  long long qs[3], ks[3];
+  take_strides(nullptr, H, Nq, d, dtype, qs);
+  take_strides(nullptr, H, Nkv, d, dtype, ks);
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  if (encode_map(&tmQ, Q, a.fp16, d, Nq, H, B, qs) != OSATTN_OK ||
+      encode_map(&tmK, K, a.fp16, d, Nkv, H, B, ks) != OSATTN_OK ||
+      encode_map(&tmV, V, a.fp16, d, Nkv, H, B, ks) != OSATTN_OK ||
+      encode_map(&tmdO, dO, a.fp16, d, Nq, H, B, qs) != OSATTN_OK)
+    return OSATTN_ERR_CUDA;
+  return osattn::launch_bwd(a, tmQ, tmK, tmV, tmdO) == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
 int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,

@@ -50,6 +50,35 @@ cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, v
                                    float* LSE, long long rows, int d, int num_splits, int fp16,
                                    cudaStream_t stream);
 
+// Arguments of one backward call after host validation (contiguous
+// [B, H, N, d] tensors; 16-bit element type).
+struct BwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const void* dO;
+  const float* LSE;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* D;  // workspace [B, H, Nq]: rowsum(dO * O)
+  int B, H, Nq, Nkv, d;
+  float scale;
+  int causal;
+  const int32_t* key_len;  // device, may be null
+  int fp16;                // 0 bf16, 1 fp16
+  cudaStream_t stream;
+  unsigned int* status;
+  uint64_t wait_limit_ns;
+  int num_sms;
+};
+
+// Backward kernels (bwd_tcgen05.cu): D = rowsum(dO * O), then dK/dV, then dQ.
+cudaError_t prepare_bwd();  // once per device: kernel attributes
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, const CUtensorMap& tmdO);
+
 // Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix;
 // elem: 0 bf16, 1 fp32, 2 fp16 (the public dtype codes).
 cudaError_t launch_softmax_rows(const void* in, void* out, float* lse, long long rows, int N,

@@ -39,6 +39,7 @@ class Workload:
     q_std: float = 1.0
     kv_std: float = 1.0
     splits: int = 0  # > 0: measured through the split-KV entry point with this many ranges
+    bwd: bool = False  # True: the backward pass (dQ, dK, dV) is measured
 
     @property
     def scale(self) -> float:
@@ -52,6 +53,12 @@ class Workload:
 
     def torch_dtype(self):
         return TORCH_DTYPES[self.dtype]
+
+    @property
+    def bwd_flops(self) -> float:
+        """Nominal backward FLOPs: the five products S, dP, dV, dK, dQ of
+        2*N*N*d each per head, 2.5 times the forward count."""
+        return 2.5 * self.flops
 
 
 WORKLOADS = {
@@ -79,6 +86,26 @@ SPLITKV_WORKLOADS = {
                  seed=5, splits=9),
     ]
 }
+
+# Backward-pass workloads: the two largest forward shapes, with an upstream
+# gradient dO ~ N(0, 1) drawn after Q, K and V from the workload's seed + 1000.
+BWD_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("bwd_bf16_b8_h40_n2048_d128", "bf16", 8, 40, 2048, 2048, 128, False, None,
+                 seed=3, bwd=True),
+        Workload("bwd_bf16_causal_b1_h32_n16384_d128_qstd3", "bf16", 1, 32, 16384, 16384, 128,
+                 True, None, seed=4, q_std=3.0, bwd=True),
+    ]
+}
+
+
+def make_grad_out(w: Workload):
+    """Upstream gradient dO [B,H,Nq,d] ~ N(0, 1) on the CPU, in the workload dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 1000)
+    return torch.randn((w.B, w.H, w.Nq, w.d), generator=g, dtype=torch.float32).to(w.torch_dtype())
+
 
 @dataclasses.dataclass(frozen=True)
 class RowWorkload:

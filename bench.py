@@ -396,6 +396,155 @@ def run_ours(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ backward
+BWD_METRIC = "attention backward TFLOPS on 1 GB300 (2.5x forward FLOPs) and % of dense BF16 peak"
+
+
+def bwd_oracle_sample(w, q, k, v, do, target_s: float):
+    """The oracle's gradients on a bounded sample of the workload: batch 0,
+    its first `heads` heads, and for a causal workload only the first n
+    query rows and keys (n grown until the call takes about a quarter of
+    target_s; a causal prefix is itself a causal problem with the same dQ
+    rows).  Returns (heads, n, dQ, dK, dV, secs, flops)."""
+    import oracle
+
+    cores = cpu_cores()
+    # A causal prefix is the same problem for its dQ rows; without the mask
+    # every row sees every key, so only whole heads are comparable.
+    heads, n = min(w.H, cores), (min(w.Nq, w.Nkv, 256) if w.causal else w.Nq)
+    while True:
+        sl = (slice(0, 1), slice(0, heads), slice(0, n))
+        t0 = time.perf_counter()
+        dQ, dK, dV = oracle.attention_bwd(q[sl], k[sl], v[sl], do[sl], w.scale, w.causal, None)
+        secs = time.perf_counter() - t0
+        flops = 10.0 * heads * n * n * w.d / (2 if w.causal else 1)
+        if secs >= target_s / 4 or n >= min(w.Nq, w.Nkv):
+            break
+        n = min(n * 2, w.Nq, w.Nkv)
+    return heads, n, dQ, dK, dV, secs, flops
+
+
+def run_bwd(args, w):
+    import numpy as np
+    import torch
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import make_grad_out, make_inputs
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    q, k, v, kl = make_inputs(w)
+    do = make_grad_out(w)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        O, L = osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(osattn.bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        osattn.bwd(qd, kd, vd, O, L, dod, scale=w.scale, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                   workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    if osattn.get_device_status(stream) != osattn.OK:
+        raise RuntimeError("device-side wait timed out during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    barrier(world)
+    if osattn.get_device_status(stream) != osattn.OK:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    local_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    total_ms = reduce_max(local_ms, world)
+    value = world * w.bwd_flops * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = w.bwd_flops / (local_ms / args.steps * 1e-3) / 1e12
+
+    # end to end: inputs (q, k, v, O, LSE, dO) in, gradients out
+    hin = [t.pin_memory() for t in (q, k, v, O.cpu(), L.cpu(), do)]
+    dins = [qd, kd, vd, O, L, dod]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    e2e_steps = max(3, min(args.steps, 20))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            flush.fill_(i & 0xFF)
+            es[i].record(stream)
+            for dsrc, h in zip(dins, hin):
+                dsrc.copy_(h, non_blocking=True)
+            step()
+            for h, g in zip(hout, (dq, dk, dv)):
+                h.copy_(g, non_blocking=True)
+            ee[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)), world) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    if rank == 0:
+        heads, n, rQ, rK, rV, secs, cflops = bwd_oracle_sample(w, q, k, v, do, args.cpu_seconds)
+        gq = dq[0:1, :heads, :n].double().cpu().numpy()
+        err = {"dQ": float(np.abs(gq - rQ).max())}
+        if n == w.Nq and n == w.Nkv:  # the sample is whole heads: dK and dV comparable too
+            err["dK"] = float(np.abs(dk[0:1, :heads].double().cpu().numpy() - rK).max())
+            err["dV"] = float(np.abs(dv[0:1, :heads].double().cpu().numpy() - rV).max())
+        err["sample"] = f"batch 0, heads 0-{heads - 1}, first {n} rows"
+        peak = float(peaks["bf16_tflops"])
+        line = {
+            "metric": BWD_METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv,
+                       "d": w.d, "causal": w.causal, "flops_per_step": w.bwd_flops,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": round(100 * value / world / peak, 2),
+            "max_abs_err": err,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "bwd_rowdot + bwd_dkdv + bwd_dq kernels, timed together",
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+            "cpu_baseline": {"value": round(cflops / secs / 1e12, 6), "unit": "TFLOPS",
+                             "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"gradients of batch 0, {heads} heads, first {n} query "
+                                       f"rows and keys of {w.name}, fp64, {secs:.1f} s"},
+            "e2e": {"value": round(world * w.bwd_flops / (e2e_ms * 1e-3) / 1e12, 3),
+                    "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps * 3,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 # ------------------------------------------------------------------ row softmax
 def run_softmax_rows(args, w):
     """The standalone online row softmax: HBM-bound, one read and one write
@@ -515,8 +664,9 @@ def run_softmax_rows(args, w):
 
 
 def main(argv=None):
-    from attention_forward_online_gb300.inputs import (BENCH_WORKLOAD, ROW_WORKLOADS,
-                                                       SPLITKV_WORKLOADS, WORKLOADS)
+    from attention_forward_online_gb300.inputs import (BENCH_WORKLOAD, BWD_WORKLOADS,
+                                                       ROW_WORKLOADS, SPLITKV_WORKLOADS,
+                                                       WORKLOADS)
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -525,7 +675,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     allw = dict(WORKLOADS, **SPLITKV_WORKLOADS)
     ap.add_argument("--workload", default=BENCH_WORKLOAD,
-                    choices=sorted(allw) + sorted(ROW_WORKLOADS))
+                    choices=sorted(allw) + sorted(ROW_WORKLOADS) + sorted(BWD_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.workload in ROW_WORKLOADS:
@@ -534,6 +684,12 @@ def main(argv=None):
                               "the reference arm is defined for the attention workloads"}))
             return 0
         return run_softmax_rows(args, ROW_WORKLOADS[args.workload])
+    if args.workload in BWD_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the reference arm is defined for the forward attention workloads"}))
+            return 0
+        return run_bwd(args, BWD_WORKLOADS[args.workload])
     w = allw[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

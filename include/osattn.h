@@ -191,6 +191,50 @@ int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void
                                void* stream);
 
 /*
+ * osattn_bwd_workspace_bytes - device workspace osattn_bwd needs: one fp32
+ * per query row (B*H*Nq floats).  Returns 0 for sizes < 1.
+ */
+size_t osattn_bwd_workspace_bytes(int B, int H, int Nq);
+
+/*
+ * osattn_bwd - gradients of osattn_fwd for an upstream gradient dO.
+ *
+ * With P_ij = e^{s_ij - LSE_i} on the visible keys J_i (s, J and LSE exactly
+ * as in osattn_fwd; the forward pass keeps LSE per row so that the backward
+ * pass can rebuild P, [Ch6] §6.5, recomputing the scores, [XXQK] §5.2):
+ *     D_i   = <dO_i, O_i>
+ *     dS_ij = P_ij (<dO_i, V_j> - D_i)
+ *     dQ_i  = scale * sum_j dS_ij K_j
+ *     dK_j  = scale * sum_i dS_ij Q_i
+ *     dV_j  = sum_i P_ij dO_i
+ * (the chain rule on the forward definition).  Rows with J empty contribute
+ * nothing; keys no row sees get dK = dV = 0.
+ *
+ *   Q, K, V   device, as for osattn_fwd (contiguous [B, H, N, d]) (read)
+ *   O, LSE    device, the outputs of osattn_fwd for these Q, K, V, scale,
+ *             causal and key_len (read)
+ *   dO        device, [B, H, Nq, d] contiguous, element type `dtype` (read)
+ *   dQ        device, [B, H, Nq, d] contiguous, element type `dtype` (written)
+ *   dK, dV    device, [B, H, Nkv, d] contiguous, element type `dtype` (written)
+ *   B .. key_len   as for osattn_fwd
+ *   dtype     OSATTN_BF16 or OSATTN_FP16 (OSATTN_FP32 -> OSATTN_ERR_UNSUPPORTED)
+ *   workspace caller-owned device memory, 16-byte aligned, at least
+ *             osattn_bwd_workspace_bytes(B, H, Nq) bytes (else
+ *             OSATTN_ERR_INVALID_ARG); overwritten, free once the stream
+ *             passes the call
+ *
+ * dO, dQ, dK, dV must be 16-byte aligned and must not overlap each other or
+ * the inputs.  Three kernels are enqueued on `stream` (D, then dK/dV, then
+ * dQ); each output element is written by one CTA, so the results do not
+ * depend on scheduling.  The call allocates nothing.  Errors as for
+ * osattn_fwd.
+ */
+int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+               const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv,
+               int d, float scale, int causal, const int32_t* key_len, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * osattn_softmax_rows - row softmax of a [rows, N] matrix with the online
  * (m, l) normaliser of [Ch6] §6.4: per row,
  *     y_i = e^{x_i - m} / l,  m = max_i x_i,  l = sum_i e^{x_i - m},

@@ -193,3 +193,36 @@ def test_binding_rejects_non_unit_inner_stride(L):
     q = torch.zeros(1, 1, 64, 4, dtype=torch.bfloat16).transpose(2, 3)  # d axis strided
     with pytest.raises(ValueError):
         osattn._bhn_strides(q)
+
+
+def call_bwd(**kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=1, H=1, Nq=8, Nkv=8, d=64,
+             scale=0.125, causal=0, key_len=None, dtype=osattn.BF16, ws=P, ws_bytes=1 << 20)
+    a.update(kw)
+    return osattn.lib().osattn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"],
+                                   a["dk"], a["dv"], a["B"], a["H"], a["Nq"], a["Nkv"], a["d"],
+                                   a["scale"], a["causal"], a["key_len"], a["dtype"], a["ws"],
+                                   a["ws_bytes"], ctypes.c_void_p(None))
+
+
+def test_bwd_workspace_size(L):
+    assert osattn.bwd_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 4
+    assert osattn.bwd_workspace_bytes(0, 3, 100) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(do=None), osattn.ERR_INVALID_ARG),
+    (dict(dq=None), osattn.ERR_INVALID_ARG),
+    (dict(dk=P + 2), osattn.ERR_INVALID_ARG),
+    (dict(dv=P + 8), osattn.ERR_INVALID_ARG),
+    (dict(o=None), osattn.ERR_INVALID_ARG),
+    (dict(lse=None), osattn.ERR_INVALID_ARG),
+    (dict(ws=None), osattn.ERR_INVALID_ARG),
+    (dict(ws_bytes=8 * 4 - 1), osattn.ERR_INVALID_ARG),
+    (dict(Nq=0), osattn.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), osattn.ERR_INVALID_ARG),
+    (dict(dtype=osattn.FP32), osattn.ERR_UNSUPPORTED),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+])
+def test_bwd_host_validation(L, kw, expect):
+    assert call_bwd(**kw) == expect
