@@ -423,9 +423,9 @@ int osattn_ref_attention_bwd(const void* Q, const void* K, const void* V, const 
       }
       double m = kNegInf;
       for (int j = 0; j < jend; ++j) m = std::max(m, s[j]);
-      double l = 0.0;
-      for (int j = 0; j < jend; ++j) l += std::exp(s[j] - m);
-      const double lse = m + std::log(l);
+      double den = 0.0;
+      for (int j = 0; j < jend; ++j) den += std::exp(s[j] - m);
+      const double lse = m + std::log(den);
       double D = 0.0;
       for (int j = 0; j < jend; ++j) {
         pr[j] = std::exp(s[j] - lse);
