@@ -21,7 +21,7 @@
 //                        dV += P^T dO   and  dK += dS^T Q     (A from tensor memory)
 //   bwd_dq_kernel      one CTA per 128-row query tile: Q and dO stay, the
 //                      visible K/V tiles stream.  Per key tile:
-//                        S = Q K^T  and  dP = dO V^T;  dS in 16-bit over S
+//                        S = Q K^T  and  dP = dO V^T;  dS in 16-bit over dP
 //                        dQ += dS K                            (A from tensor memory)
 // S and dP are computed twice (once per kernel) so that no kernel needs
 // atomics: each output element is written once, by one CTA.
@@ -33,9 +33,9 @@
 // forward kernel: a wait past the limit records OSATTN_ERR_TIMEOUT, the CTA
 // drains its own copies and MMAs, frees tensor memory and returns.
 //
-// Tensor memory (512 columns): [0, 128) S or S^T (then P / dS packed in its
-// first 64 columns), [128, 256) dP or dP^T (dS^T packed in its first 64),
-// [256, 256 + d) dV or dQ, [256 + d, 256 + 2d) dK.
+// Tensor memory (512 columns): [0, 128) S or S^T, [128, 256) dP or dP^T
+// (each as two 64-column halves; P^T and dS are packed over the first 32
+// columns of their half), [256, 256 + d) dV or dQ, [256 + d, 256 + 2d) dK.
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -71,8 +71,8 @@ struct BwdCfg {
 struct __align__(8) BwdBars {
   uint64_t fixed_full;            // the tile pair loaded once (K, V or Q, dO)
   uint64_t full[4], empty[4];     // ring stages
-  uint64_t sd_full;               // MMA -> elementwise: the two score tiles are ready
-  uint64_t p_full;                // elementwise -> MMA: the 16-bit operands are written (128)
+  uint64_t sd_full[2];            // MMA -> elementwise: half x of both score tiles is ready
+  uint64_t p_full[2];             // elementwise -> MMA: half x's 16-bit operands are written (128)
   uint64_t acc_full;              // MMA -> epilogue: the last accumulation is done
   uint64_t mma_drain;
   uint32_t tmem_base;
@@ -183,6 +183,48 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O
   }
 }
 
+// Both kernels split every 128-column score tile into two 64-column halves
+// h = 0, 1 with their own barriers: while the elementwise warps turn half h
+// into 16-bit operands, the tensor core computes the other half or
+// accumulates the one finished before, so the MMAs of a tile overlap its
+// elementwise work.  Score half h sits at tensor-memory column 64h (S or
+// S^T) and 128 + 64h (dP or dP^T); the 16-bit results are written over the
+// first 32 columns of those halves: P^T over S^T's (dK/dV kernel only) and
+// dS over dP's.
+
+// Elementwise pass over one 64-column half: two chunks of 32.  `first` is
+// the index (query for dK/dV, key for dQ) of the half's column 0.
+template <bool kF16, bool kWriteP, typename Vis, typename Col>
+__device__ __forceinline__ void bwd_half(uint32_t s_addr, uint32_t dp_addr, float c, Vis&& vis,
+                                         Col&& col) {
+#pragma unroll 1
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t sv[32], dv[32];
+    tmem_ld_32x32b_x32(s_addr + ch * 32, sv);
+    tmem_ld_32x32b_x32(dp_addr + ch * 32, dv);
+    tmem_ld_wait();
+    reg_fence32(sv);
+    reg_fence32(dv);
+    uint32_t pk[16], gk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float pr[2], gr[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int x = ch * 32 + 2 * e + u;  // column within the half
+        float l2, dd;
+        col(x, l2, dd);
+        pr[u] = vis(x) ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), c, -l2)) : 0.f;
+        gr[u] = pr[u] * (__uint_as_float(dv[2 * e + u]) - dd);
+      }
+      if (kWriteP) pk[e] = pack2<kF16>(pr[0], pr[1]);
+      gk[e] = pack2<kF16>(gr[0], gr[1]);
+    }
+    if (kWriteP) tmem_st_32x32b_x16(s_addr + ch * 16, pk);
+    tmem_st_32x32b_x16(dp_addr + ch * 16, gk);
+  }
+}
+
 // ------------------------------------------------------------------ dK, dV
 template <int HD, bool kF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -216,8 +258,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->sd_full[x], 1);
+      mbar_init(&bars->p_full[x], 128);
+    }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
@@ -288,27 +332,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
+    // Order: S^T_0, dP^T_0, S^T_1, dP^T_1 of tile 0; then per tile it and
+    // half x: dV, dK += (half x of it), then S^T_x, dP^T_x of tile it + 1.
     if (lane == 0 && n_it > 0) {
       const uint64_t kA = sdesc_sw128(smem_u32(sK), 16, 1024);  // K-major A
       const uint64_t vA = sdesc_sw128(smem_u32(sV), 16, 1024);
+      constexpr uint32_t kHalfRows = 64 * 128 >> 4;             // 64 rows of a column block
       bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t sq = smem_u32(ring), sdo = sq + C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          mma_abt<64, HD, kF16>(tmem + 64 * x, kA, sdesc_add(sdesc_sw128(sq, 16, 1024), x * kHalfRows));
+          mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, vA,
+                                sdesc_add(sdesc_sw128(sdo, 16, 1024), x * kHalfRows));
+          mma_commit(&bars->sd_full[x]);
+        }
+      }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::kStages;
-        ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after_sync();
+        const int s = it % C::kStages, s1 = (it + 1) % C::kStages;
         const uint32_t sq = smem_u32(ring + s * C::kStageBytes), sdo = sq + C::kTileBytes;
-        mma_abt_128<HD, kF16>(tmem, kA, sdesc_sw128(sq, 16, 1024));         // S^T = K Q^T
-        mma_abt_128<HD, kF16>(tmem + 128, vA, sdesc_sw128(sdo, 16, 1024));  // dP^T = V dO^T
-        mma_commit(&bars->sd_full);
-        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after_sync();
-        // dV += P^T dO and dK += dS^T Q: B read MN-major from the same tiles
-        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sdo, kT * 128, 1024), it > 0);
-        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc1, tmem + 128, sdesc_sw128(sq, kT * 128, 1024),
-                                 it > 0);
-        mma_commit(&bars->empty[s]);
+        const uint32_t nq = smem_u32(ring + s1 * C::kStageBytes), ndo = nq + C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          ok = mbar_wait(&bars->p_full[x], static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // dV += P^T dO and dK += dS^T Q over the 64 queries of half x: B
+          // read MN-major from those 64 rows of the tiles
+          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc0, tmem + 64 * x,
+                                  sdesc_add(sdesc_sw128(sdo, kT * 128, 1024), x * kHalfRows),
+                                  it > 0 || x > 0);
+          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc1, tmem + 128 + 64 * x,
+                                  sdesc_add(sdesc_sw128(sq, kT * 128, 1024), x * kHalfRows),
+                                  it > 0 || x > 0);
+          if (x == 1) mma_commit(&bars->empty[s]);
+          if (it + 1 < n_it) {
+            if (x == 0) {
+              ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
+                             kSiteBwdMma);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+            mma_abt<64, HD, kF16>(tmem + 64 * x, kA, sdesc_add(sdesc_sw128(nq, 16, 1024), x * kHalfRows));
+            mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, vA,
+                                  sdesc_add(sdesc_sw128(ndo, 16, 1024), x * kHalfRows));
+            mma_commit(&bars->sd_full[x]);
+          }
+        }
       }
       if (ok) mma_commit(&bars->acc_full);
       // Every MMA this thread issued must complete before tensor memory is freed.
@@ -321,48 +394,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kabs = k0 + row;
     const bool row_live = kabs < kv_len;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float c = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0; ok && it < n_it; ++it) {
       const int s = it % C::kStages;
-      ok = mbar_wait(&bars->sd_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
-      // LSE and D of this query tile were staged with the stage's loads.
-      if (ok) ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdElem);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
       const int q0 = (it0 + it) * kT;
-      const float* l2 = bars->lse2[s];
-      const float* dd = bars->dsum[s];
-#pragma unroll 1
-      for (int ch = 0; ch < kT / 32; ++ch) {
-        uint32_t sv[32], dv[32];
-        tmem_ld_32x32b_x32(lane_base + ch * 32, sv);
-        tmem_ld_32x32b_x32(lane_base + 128 + ch * 32, dv);
-        tmem_ld_wait();
-        reg_fence32(sv);
-        reg_fence32(dv);
-        uint32_t pk[16], gk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pr[2], gr[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = ch * 32 + 2 * e + u;
-            const bool vis = row_live && (!p.causal || kabs <= q0 + qq);
-            const float x = fmaf(__uint_as_float(sv[2 * e + u]), c, -l2[qq]);
-            pr[u] = vis ? ex2_approx(x) : 0.f;
-            gr[u] = pr[u] * (__uint_as_float(dv[2 * e + u]) - dd[qq]);
-          }
-          pk[e] = pack2<kF16>(pr[0], pr[1]);
-          gk[e] = pack2<kF16>(gr[0], gr[1]);
-        }
-        tmem_st_32x32b_x16(lane_base + ch * 16, pk);
-        tmem_st_32x32b_x16(lane_base + 128 + ch * 16, gk);
+      for (int x = 0; x < 2; ++x) {
+        ok = mbar_wait(&bars->sd_full[x], static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
+        // LSE and D of this query tile were staged with the stage's loads.
+        if (ok && x == 0)
+          ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdElem);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const float* l2 = bars->lse2[s] + 64 * x;
+        const float* dd = bars->dsum[s] + 64 * x;
+        const int qx = q0 + 64 * x;
+        bwd_half<kF16, true>(
+            lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
+            [&](int col) { return row_live && (!p.causal || kabs <= qx + col); },
+            [&](int col, float& L2, float& D) {
+              L2 = l2[col];
+              D = dd[col];
+            });
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars->p_full[x]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bars->p_full);
     }
     // epilogue: dV = sum P^T dO, dK = scale * sum dS^T Q
     bool has_acc = false;
@@ -423,8 +480,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->sd_full[x], 1);
+      mbar_init(&bars->p_full[x], 128);
+    }
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
@@ -469,25 +528,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         drain(&bars->full[j % C::kStages], static_cast<uint32_t>(j / C::kStages) & 1u, wc.limit_ns);
     }
   } else if (warp == kMmaWarp) {
+    // Order: S_0, dP_0, S_1, dP_1 of key tile 0; then per key tile j and
+    // half x: dQ += dS_x K_x, then S_x, dP_x of key tile j + 1.
     if (lane == 0 && n_kt > 0) {
       const uint64_t qA = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dA = sdesc_sw128(smem_u32(sdO), 16, 1024);
+      constexpr uint32_t kHalfRows = 64 * 128 >> 4;
       bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t sk = smem_u32(ring), sv = sk + C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          mma_abt<64, HD, kF16>(tmem + 64 * x, qA, sdesc_add(sdesc_sw128(sk, 16, 1024), x * kHalfRows));
+          mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, dA,
+                                sdesc_add(sdesc_sw128(sv, 16, 1024), x * kHalfRows));
+          mma_commit(&bars->sd_full[x]);
+        }
+      }
       for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % C::kStages;
-        ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(j / C::kStages) & 1u, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const uint32_t sk = smem_u32(ring + s * C::kStageBytes), sv = sk + C::kTileBytes;
-        mma_abt_128<HD, kF16>(tmem, qA, sdesc_sw128(sk, 16, 1024));        // S = Q K^T
-        mma_abt_128<HD, kF16>(tmem + 128, dA, sdesc_sw128(sv, 16, 1024));  // dP = dO V^T
-        mma_commit(&bars->sd_full);
-        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
-        if (!ok) break;
-        tc_fence_after_sync();
-        // dQ += dS K: K read MN-major from the same tile
-        mma_tmem_a_128<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sk, kT * 128, 1024), j > 0);
-        mma_commit(&bars->empty[s]);
+        const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
+        const uint32_t sk = smem_u32(ring + s * C::kStageBytes);
+        const uint32_t nk = smem_u32(ring + s1 * C::kStageBytes), nv = nk + C::kTileBytes;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          ok = mbar_wait(&bars->p_full[x], static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // dQ += dS K over the 64 keys of half x (dS over dP's half): K read
+          // MN-major from those keys
+          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc0, tmem + 128 + 64 * x,
+                                  sdesc_add(sdesc_sw128(sk, kT * 128, 1024), x * kHalfRows),
+                                  j > 0 || x > 0);
+          if (x == 1) mma_commit(&bars->empty[s]);
+          if (j + 1 < n_kt) {
+            if (x == 0) {
+              ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((j + 1) / C::kStages) & 1u, wc,
+                             kSiteBwdMma);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+            mma_abt<64, HD, kF16>(tmem + 64 * x, qA, sdesc_add(sdesc_sw128(nk, 16, 1024), x * kHalfRows));
+            mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, dA,
+                                  sdesc_add(sdesc_sw128(nv, 16, 1024), x * kHalfRows));
+            mma_commit(&bars->sd_full[x]);
+          }
+        }
       }
       if (ok) mma_commit(&bars->acc_full);
       mma_commit(&bars->mma_drain);
@@ -505,40 +592,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       Dq = p.D[rix];
     }
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float c = p.scale_log2;
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      ok = mbar_wait(&bars->sd_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const int kb = j * kT;
-#pragma unroll 1
-      for (int ch = 0; ch < kT / 32; ++ch) {
-        uint32_t sv[32], dv[32];
-        tmem_ld_32x32b_x32(lane_base + ch * 32, sv);
-        tmem_ld_32x32b_x32(lane_base + 128 + ch * 32, dv);
-        tmem_ld_wait();
-        reg_fence32(sv);
-        reg_fence32(dv);
-        uint32_t gk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float gr[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int k = kb + ch * 32 + 2 * e + u;
-            const bool vis = k < kv_len && (!p.causal || k <= q);
-            const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), c, -l2)) : 0.f;
-            gr[u] = pr * (__uint_as_float(dv[2 * e + u]) - Dq);
-          }
-          gk[e] = pack2<kF16>(gr[0], gr[1]);
-        }
-        tmem_st_32x32b_x16(lane_base + ch * 16, gk);
+    for (int j = 0; ok && j < n_kt; ++j) {
+      for (int x = 0; x < 2; ++x) {
+        ok = mbar_wait(&bars->sd_full[x], static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int kx = j * kT + 64 * x;
+        bwd_half<kF16, false>(
+            lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
+            [&](int col) { return kx + col < kv_len && (!p.causal || kx + col <= q); },
+            [&](int, float& L2, float& D) {
+              L2 = l2;
+              D = Dq;
+            });
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars->p_full[x]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bars->p_full);
     }
     bool has_acc = false;
     if (ok && n_kt > 0) {

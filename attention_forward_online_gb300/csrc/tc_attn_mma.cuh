@@ -12,13 +12,14 @@
 
 namespace osattn {
 
-// D (128 x 128 fp32, tensor memory) = A B^T over KD elements of the inner
-// axis: A and B are 128-row K-major tiles (a_desc / b_desc address their
-// first 16-element slice; later slices move 32 bytes within a swizzle row,
-// or to the next 64-column block).  Eight MMAs of K = 16 for KD = 128.
-template <int KD, bool kF16>
-__device__ __forceinline__ void mma_abt_128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
-  constexpr uint32_t id = idesc_f16_f32(128, 128, 0, kF16);  // K-major A and B
+// D (128 x N fp32, tensor memory) = A B^T over KD elements of the inner
+// axis: A is a 128-row and B an N-row K-major tile (a_desc / b_desc address
+// their first 16-element slice; later slices move 32 bytes within a swizzle
+// row, or to the next 64-column block, 128 rows = 16 KB on).  B may be a
+// row range of a 128-row tile: the block offsets are those of the tile.
+template <int N, int KD, bool kF16>
+__device__ __forceinline__ void mma_abt(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t id = idesc_f16_f32(128, N, 0, kF16);  // K-major A and B
   mma_ss_k<0>(d_tmem, a_desc, b_desc, id);
 #pragma unroll
   for (int kk = 1; kk < KD / 16; ++kk) {
@@ -27,19 +28,32 @@ __device__ __forceinline__ void mma_abt_128(uint32_t d_tmem, uint64_t a_desc, ui
   }
 }
 
-// D (128 x N fp32) (+)= A B over 128 inner elements: A from tensor memory
-// (a 128 x 128 16-bit tile packed in pairs over 64 columns), B a 128-row
-// MN-major shared-memory tile (b_desc: leading offset = distance between its
-// 64-column blocks); 16 inner elements per MMA = two 8-row swizzle atoms.
-template <int N, bool kF16>
-__device__ __forceinline__ void mma_tmem_a_128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                               bool accumulate) {
+template <int KD, bool kF16>
+__device__ __forceinline__ void mma_abt_128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  mma_abt<128, KD, kF16>(d_tmem, a_desc, b_desc);
+}
+
+// D (128 x N fp32) (+)= A B over 16 * KSTEPS inner elements: A from tensor
+// memory (16-bit pairs, 8 columns per 16 elements), B an MN-major
+// shared-memory tile read from its row b_desc points at (leading offset =
+// distance between its 64-column blocks); 16 inner elements per MMA = two
+// 8-row swizzle atoms (2 KB).
+template <int N, int KSTEPS, bool kF16>
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           bool accumulate) {
   constexpr uint32_t id = idesc_f16_f32(128, N, 1, kF16);  // B is MN-major
   mma_bf16_ts(d_tmem, a_tmem, b_desc, id, accumulate ? 1u : 0u);
 #pragma unroll
-  for (int kk = 1; kk < 128 / 16; ++kk)
+  for (int kk = 1; kk < KSTEPS; ++kk)
     mma_ts_k<1>(d_tmem, a_tmem + kk * 8, sdesc_add(b_desc, static_cast<uint32_t>((kk * 2048) >> 4)),
                 id);
+}
+
+// The forward's P V: A a 128 x 128 tile (64 columns of pairs).
+template <int N, bool kF16>
+__device__ __forceinline__ void mma_tmem_a_128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               bool accumulate) {
+  mma_tmem_a<N, 8, kF16>(d_tmem, a_tmem, b_desc, accumulate);
 }
 
 }  // namespace osattn
