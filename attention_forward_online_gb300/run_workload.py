@@ -5,8 +5,10 @@
 
 Inputs are the seeded synthetic tensors of the named workload, resident on
 cuda:0 before the first launch; --heads keeps only the first H heads (a
-smaller case of the same kernel for detailed Nsight Compute captures).
-Prints the mean launch time from CUDA events on the launching stream.
+smaller case of the same kernel for detailed Nsight Compute captures).  A
+backward workload runs the forward pass once, untimed, and then times the
+backward call (its three kernels).  Prints the median launch time from
+CUDA events on the launching stream.
 """
 import argparse
 import dataclasses
@@ -22,9 +24,10 @@ def main(argv=None):
     import torch
 
     from attention_forward_online_gb300 import osattn
-    from attention_forward_online_gb300.inputs import SPLITKV_WORKLOADS, WORKLOADS, make_inputs
+    from attention_forward_online_gb300.inputs import (BWD_WORKLOADS, SPLITKV_WORKLOADS, WORKLOADS,
+                                                       make_grad_out, make_inputs)
 
-    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS)
+    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS, **BWD_WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", required=True, choices=sorted(allw))
     ap.add_argument("--launches", type=int, default=4)
@@ -48,11 +51,20 @@ def main(argv=None):
     if w.splits:
         ws = torch.empty(osattn.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, w.splits),
                          dtype=torch.uint8, device=dev)
+    if w.bwd:
+        dod = make_grad_out(w).to(dev)
+        osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, key_len=kld, out=O, lse=L, stream=s)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws = torch.empty(osattn.bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.launches)]
+    flops = w.bwd_flops if w.bwd else w.flops
     with torch.cuda.stream(s):
         for i in range(args.launches):
             ev[2 * i].record(s)
-            if w.splits:
+            if w.bwd:
+                osattn.bwd(qd, kd, vd, O, L, dod, scale=w.scale, causal=w.causal, key_len=kld,
+                           dq=dq, dk=dk, dv=dv, workspace=ws, stream=s)
+            elif w.splits:
                 osattn.fwd_splitkv(qd, kd, vd, w.splits, scale=w.scale, causal=w.causal,
                                    key_len=kld, out=O, lse=L, workspace=ws, stream=s)
             else:
@@ -65,10 +77,9 @@ def main(argv=None):
         print("device status:", osattn.status_string(st))
         return 1
     ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.launches)]
-    tf = [w.flops / (m * 1e-3) / 1e12 for m in ms]
     med = sorted(ms[1:] if len(ms) > 1 else ms)[len(ms[1:] if len(ms) > 1 else ms) // 2]
     print(f"{w.name} H={w.H} splits={w.splits}: launches {args.launches}, median {med:.4f} ms = "
-          f"{w.flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
+          f"{flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
           f"ms {['%.4f' % m for m in ms]}")
     return 0
 

@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOPS on 1 GB300 and % of dense BF16 tensor peak; max-abs err vs oracle"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ("fwd_bf16_tcgen05.cu", "sm100_ptx.cuh")
+KERNEL_SOURCES = ("fwd_bf16_tcgen05.cu", "sm100_ptx.cuh", "tc_attn_mma.cuh")
 
 
 def load_peaks():
