@@ -90,6 +90,7 @@ struct BwdParams {
   uint16_t* dQ;
   uint16_t* dK;
   uint16_t* dV;
+  long long dq_s[3], dk_s[3], dv_s[3];  // element strides of the b, h and row axes
   const float* LSE;
   const float* D;
   const int32_t* key_len;
@@ -161,17 +162,23 @@ __device__ __forceinline__ float2 load2<__half>(const __half* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
+struct RowStrides {
+  long long o[3], g[3];  // element strides of the b, h and row axes of O and dO
+};
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O,
                                                          const T* __restrict__ dO,
                                                          float* __restrict__ D, long long rows,
-                                                         int d) {
+                                                         int d, int H, int Nq, RowStrides st) {
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        row < rows; row += warps) {
-    const T* o = O + row * d;
-    const T* g = dO + row * d;
+    const long long bh = row / Nq;
+    const long long i = row - bh * Nq, b = bh / H, h = bh - b * H;
+    const T* o = O + b * st.o[0] + h * st.o[1] + i * st.o[2];
+    const T* g = dO + b * st.g[0] + h * st.g[1] + i * st.g[2];
     float acc = 0.f;
     for (int c = 2 * lane; c < d; c += 64) {
       const float2 a = load2<T>(o + c), b = load2<T>(g + c);
@@ -431,9 +438,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       const bool store = kabs < p.Nkv;
-      const long long off = (static_cast<long long>(bh) * p.Nkv + kabs) * HD;
-      write_row<HD, kF16>(p.dV + off, lane_base + C::kColAcc0, has_acc, store, 1.f);
-      write_row<HD, kF16>(p.dK + off, lane_base + C::kColAcc1, has_acc, store, p.scale);
+      write_row<HD, kF16>(p.dV + b * p.dv_s[0] + h * p.dv_s[1] + kabs * p.dv_s[2],
+                          lane_base + C::kColAcc0, has_acc, store, 1.f);
+      write_row<HD, kF16>(p.dK + b * p.dk_s[0] + h * p.dk_s[1] + kabs * p.dk_s[2],
+                          lane_base + C::kColAcc1, has_acc, store, p.scale);
     }
   }
 
@@ -619,7 +627,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) tc_fence_after_sync();
       has_acc = ok;
     }
-    if (ok) write_row<HD, kF16>(p.dQ + rix * HD, lane_base + C::kColAcc0, has_acc, row_live, p.scale);
+    if (ok)
+      write_row<HD, kF16>(p.dQ + b * p.dq_s[0] + h * p.dq_s[1] + q * p.dq_s[2],
+                          lane_base + C::kColAcc0, has_acc, row_live, p.scale);
   }
 
   __syncwarp();
@@ -649,8 +659,14 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
   const long long want = static_cast<long long>(a.num_sms) * 16;
   const int rgrid = static_cast<int>((rows + 7) / 8 < want ? (rows + 7) / 8 : want);
   using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
+  RowStrides rs;
+  for (int i = 0; i < 3; ++i) {
+    rs.o[i] = a.o_strides[i];
+    rs.g[i] = a.do_strides[i];
+  }
   bwd_rowdot_kernel<T><<<rgrid, 256, 0, a.stream>>>(static_cast<const T*>(a.O),
-                                                    static_cast<const T*>(a.dO), a.D, rows, a.d);
+                                                    static_cast<const T*>(a.dO), a.D, rows, a.d,
+                                                    a.H, a.Nq, rs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   BwdParams pk = base;
@@ -685,6 +701,11 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorM
   p.dQ = static_cast<uint16_t*>(a.dQ);
   p.dK = static_cast<uint16_t*>(a.dK);
   p.dV = static_cast<uint16_t*>(a.dV);
+  for (int i = 0; i < 3; ++i) {
+    p.dq_s[i] = a.dq_strides[i];
+    p.dk_s[i] = a.dk_strides[i];
+    p.dv_s[i] = a.dv_strides[i];
+  }
   p.LSE = a.LSE;
   p.D = a.D;
   p.key_len = a.key_len;

@@ -307,10 +307,14 @@ size_t osattn_bwd_workspace_bytes(int B, int H, int Nq) {
   return static_cast<size_t>(B) * H * Nq * sizeof(float);
 }
 
-int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-               const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv,
-               int d, float scale, int causal, const int32_t* key_len, int dtype,
-               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv, int d,
+             const int64_t* const* strides, float scale, int causal, const int32_t* key_len,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
   if (rc != OSATTN_OK) return rc;
   if (!dO || !dQ || !dK || !dV || !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) ||
@@ -320,8 +324,14 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < osattn_bwd_workspace_bytes(B, H, Nq))
     return OSATTN_ERR_INVALID_ARG;
-  DeviceState* st = nullptr;
-  rc = device_state(&st);
+  // strides: Q, K, V, O, dO, dQ, dK, dV (null array or null entries: contiguous)
+  long long st[8][3];
+  const int rows_of[8] = {Nq, Nkv, Nkv, Nq, Nq, Nq, Nkv, Nkv};
+  for (int i = 0; i < 8; ++i)
+    if (take_strides(strides ? strides[i] : nullptr, H, rows_of[i], d, dtype, st[i]) != OSATTN_OK)
+      return OSATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
   if (rc != OSATTN_OK) return rc;
   osattn::BwdArgs a;
   a.Q = Q;
@@ -344,19 +354,47 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
   a.key_len = key_len;
   a.fp16 = dtype == OSATTN_FP16;
   a.stream = static_cast<cudaStream_t>(stream);
-  a.status = st->status;
+  a.status = ds->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
-  a.num_sms = st->num_sms;
-  long long qs[3], ks[3];
-  take_strides(nullptr, H, Nq, d, dtype, qs);
-  take_strides(nullptr, H, Nkv, d, dtype, ks);
+  a.num_sms = ds->num_sms;
+  long long* dst[8] = {a.q_strides, a.k_strides, a.v_strides, a.o_strides, a.do_strides,
+                       a.dq_strides, a.dk_strides, a.dv_strides};
+  for (int i = 0; i < 8; ++i)
+    for (int j = 0; j < 3; ++j) dst[i][j] = st[i][j];
   CUtensorMap tmQ, tmK, tmV, tmdO;
-  if (encode_map(&tmQ, Q, a.fp16, d, Nq, H, B, qs) != OSATTN_OK ||
-      encode_map(&tmK, K, a.fp16, d, Nkv, H, B, ks) != OSATTN_OK ||
-      encode_map(&tmV, V, a.fp16, d, Nkv, H, B, ks) != OSATTN_OK ||
-      encode_map(&tmdO, dO, a.fp16, d, Nq, H, B, qs) != OSATTN_OK)
+  if (encode_map(&tmQ, Q, a.fp16, d, Nq, H, B, st[0]) != OSATTN_OK ||
+      encode_map(&tmK, K, a.fp16, d, Nkv, H, B, st[1]) != OSATTN_OK ||
+      encode_map(&tmV, V, a.fp16, d, Nkv, H, B, st[2]) != OSATTN_OK ||
+      encode_map(&tmdO, dO, a.fp16, d, Nq, H, B, st[4]) != OSATTN_OK)
     return OSATTN_ERR_CUDA;
   return osattn::launch_bwd(a, tmQ, tmK, tmV, tmdO) == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+               const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv,
+               int d, float scale, int causal, const int32_t* key_len, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, d, nullptr, scale, causal,
+                  key_len, dtype, workspace, workspace_bytes, stream);
+}
+
+int osattn_bwd_strided(const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                       int H, int Nq, int Nkv, int d, const int64_t* q_strides,
+                       const int64_t* k_strides, const int64_t* v_strides,
+                       const int64_t* o_strides, const int64_t* do_strides,
+                       const int64_t* dq_strides, const int64_t* dk_strides,
+                       const int64_t* dv_strides, float scale, int causal,
+                       const int32_t* key_len, int dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  const int64_t* st[8] = {q_strides, k_strides, v_strides, o_strides,
+                          do_strides, dq_strides, dk_strides, dv_strides};
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, d, st, scale, causal, key_len,
+                  dtype, workspace, workspace_bytes, stream);
 }
 
 int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,

@@ -50,8 +50,8 @@ cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, v
                                    float* LSE, long long rows, int d, int num_splits, int fp16,
                                    cudaStream_t stream);
 
-// Arguments of one backward call after host validation (contiguous
-// [B, H, N, d] tensors; 16-bit element type).
+// Arguments of one backward call after host validation ([B, H, N, d]
+// tensors with the strides below; 16-bit element type).
 struct BwdArgs {
   const void* Q;
   const void* K;
@@ -72,6 +72,9 @@ struct BwdArgs {
   unsigned int* status;
   uint64_t wait_limit_ns;
   int num_sms;
+  // Element strides of the b, h and row axes (the d axis is contiguous).
+  long long q_strides[3], k_strides[3], v_strides[3], o_strides[3], do_strides[3],
+      dq_strides[3], dk_strides[3], dv_strides[3];
 };
 
 // Backward kernels (bwd_tcgen05.cu): D = rowsum(dO * O), then dK/dV, then dQ.

@@ -29,7 +29,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
            "osattn_splitkv_workspace_bytes", "osattn_fwd_splitkv_noalloc",
-           "osattn_bwd", "osattn_bwd_workspace_bytes", "osattn_softmax_rows",
+           "osattn_bwd", "osattn_bwd_strided", "osattn_bwd_workspace_bytes", "osattn_softmax_rows",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -73,6 +73,9 @@ def lib():
             L.osattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, vp, i32, vp, ctypes.c_size_t, vp]
             L.osattn_bwd.restype = i32
+            L.osattn_bwd_strided.argtypes = ([vp] * 9 + [i32] * 5 + [i64p] * 8 +
+                                             [ctypes.c_float, i32, vp, i32, vp, ctypes.c_size_t, vp])
+            L.osattn_bwd_strided.restype = i32
             L.osattn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
             L.osattn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_softmax_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, vp]
@@ -255,16 +258,22 @@ def bwd(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False, k
         dq=None, dk=None, dv=None, workspace=None, stream=None):
     """dQ, dK, dV of the attention forward for the upstream gradient `do`.
 
-    q, k, v, o, do: contiguous CUDA bf16 or fp16 tensors ([B,H,Nq,d] for q, o,
-    do; [B,H,Nkv,d] for k, v); lse: the fp32 [B,H,Nq] LSE that fwd() returned
-    for the same inputs.  Outputs may be given preallocated; `workspace` (a
-    CUDA uint8 tensor of at least bwd_workspace_bytes(B, H, Nq) bytes) too."""
+    q, k, v, o, do: CUDA bf16 or fp16 tensors ([B,H,Nq,d] for q, o, do;
+    [B,H,Nkv,d] for k, v), any views whose last axis is contiguous; lse: the
+    contiguous fp32 [B,H,Nq] LSE that fwd() returned for the same inputs.
+    Contiguous tensors go through osattn_bwd, others through
+    osattn_bwd_strided.  Outputs may be given preallocated (any such views);
+    `workspace` (a CUDA uint8 tensor of at least bwd_workspace_bytes(B, H,
+    Nq) bytes) too."""
     import torch
 
-    B, H, Nq, Nkv, d = _check_qkv(q, k, v)
+    B, H, Nq, Nkv, d = _shapes(q, k, v)
+    dtype = _dtype_code(q)
+    if dtype == FP32:
+        raise TypeError("the backward pass takes bf16 or fp16 tensors")
     for t in (o, do):
-        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("o and do must be contiguous CUDA tensors shaped and typed like q")
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda:
+            raise ValueError("o and do must be CUDA tensors shaped and typed like q")
     if tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be fp32 [B, H, Nq]")
     if scale is None:
@@ -272,17 +281,27 @@ def bwd(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False, k
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for t, ref in ((dq, q), (dk, k), (dv, v)):
+        if t.shape != ref.shape or t.dtype != ref.dtype or not t.is_cuda:
+            raise ValueError("dq, dk, dv must be CUDA tensors shaped and typed like q, k, v")
     need = bwd_workspace_bytes(B, H, Nq)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     key_len, kl_ptr = _key_len_ptr(key_len, B)
-    st = lib().osattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq,
-                          Nkv, d, float(scale), int(bool(causal)), kl_ptr, _dtype_code(q),
-                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                          _stream_handle(stream))
+    ts = (q, k, v, o, do, dq, dk, dv)
+    ptrs = [t.data_ptr() for t in ts]
+    tail = (float(scale), int(bool(causal)), kl_ptr, dtype, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if all(t.is_contiguous() for t in ts):
+        st = lib().osattn_bwd(*ptrs[:5], lse.data_ptr(), *ptrs[5:], B, H, Nq, Nkv, d, *tail)
+        what = "osattn_bwd"
+    else:
+        strides = [_bhn_strides(t) for t in ts]
+        st = lib().osattn_bwd_strided(*ptrs[:5], lse.data_ptr(), *ptrs[5:], B, H, Nq, Nkv, d,
+                                      *strides, *tail)
+        what = "osattn_bwd_strided"
     if st != OK:
-        raise OsattnError(st, "osattn_bwd")
+        raise OsattnError(st, what)
     return dq, dk, dv
 
 

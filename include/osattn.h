@@ -235,6 +235,32 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * osattn_bwd_strided - osattn_bwd on tensors with arbitrary strides (e.g.
+ * the [B, N, H, d] layout), without transposing copies.  Same computation,
+ * results and errors as osattn_bwd.
+ *
+ *   q_strides .. dv_strides
+ *            host int64[3] each, or NULL: element strides of the B, H and
+ *            sequence axes of Q, K, V, O, dO, dQ, dK and dV (the d axis
+ *            always has stride 1; NULL means the contiguous [B, H, N, d]
+ *            layout, so osattn_bwd is this call with eight NULLs).  Each
+ *            stride must be >= 1, a multiple of 16 bytes (8 elements) and
+ *            below 2^40 bytes; otherwise OSATTN_ERR_INVALID_ARG.  Read during
+ *            the call only.  Distinct rows of dQ, dK and dV must not share
+ *            memory, and the outputs must not overlap the inputs.
+ *   LSE      always [B, H, Nq] contiguous fp32.
+ */
+int osattn_bwd_strided(const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                       int H, int Nq, int Nkv, int d, const int64_t* q_strides,
+                       const int64_t* k_strides, const int64_t* v_strides,
+                       const int64_t* o_strides, const int64_t* do_strides,
+                       const int64_t* dq_strides, const int64_t* dk_strides,
+                       const int64_t* dv_strides, float scale, int causal,
+                       const int32_t* key_len, int dtype, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * osattn_softmax_rows - row softmax of a [rows, N] matrix with the online
  * (m, l) normaliser of [Ch6] §6.4: per row,
  *     y_i = e^{x_i - m} / l,  m = max_i x_i,  l = sum_i e^{x_i - m},

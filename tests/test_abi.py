@@ -226,3 +226,33 @@ def test_bwd_workspace_size(L):
 ])
 def test_bwd_host_validation(L, kw, expect):
     assert call_bwd(**kw) == expect
+
+
+def call_bwd_strided(strides=(None,) * 8, **kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, B=1, H=2, Nq=8, Nkv=8, d=64,
+             scale=0.125, causal=0, key_len=None, dtype=osattn.BF16, ws=P, ws_bytes=1 << 20)
+    a.update(kw)
+    arrs = [None if s is None else (ctypes.c_int64 * 3)(*s) for s in strides]
+    return osattn.lib().osattn_bwd_strided(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"],
+                                           a["dq"], a["dk"], a["dv"], a["B"], a["H"], a["Nq"],
+                                           a["Nkv"], a["d"], *arrs, a["scale"], a["causal"],
+                                           a["key_len"], a["dtype"], a["ws"], a["ws_bytes"],
+                                           ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("slot", range(8))
+@pytest.mark.parametrize("bad", [(0, 64, 128), (1024, -64, 128), (1024, 64, 132), (1 << 40, 64, 128)])
+def test_bwd_strided_host_validation(L, slot, bad):
+    # Every one of the eight stride arrays (Q, K, V, O, dO, dQ, dK, dV) is
+    # checked: zero, negative, not a 16-byte multiple, >= 2^40 bytes.
+    strides = [BNHD] * 8
+    strides[slot] = bad
+    assert call_bwd_strided(strides) == osattn.ERR_INVALID_ARG
+
+
+def test_bwd_strided_shares_osattn_bwd_checks(L):
+    assert call_bwd_strided(do=None) == osattn.ERR_INVALID_ARG
+    assert call_bwd_strided(ws_bytes=2 * 8 * 4 - 1) == osattn.ERR_INVALID_ARG
+    assert call_bwd_strided(dtype=osattn.FP32) == osattn.ERR_UNSUPPORTED
+    assert call_bwd_strided(d=96) == osattn.ERR_UNSUPPORTED
+    assert call_bwd_strided((BNHD,) * 8, dv=P + 8) == osattn.ERR_INVALID_ARG

@@ -144,3 +144,36 @@ def test_bwd_full_size_workloads_sampled_heads():
             out.append(check_grad(dk[sl].double().cpu().numpy(), rk, "bf16", "dK"))
             out.append(check_grad(dv[sl].double().cpu().numpy(), rv, "bf16", "dV"))
         print(name, "max err / rms:", out)
+
+
+def _bnhd(t):
+    """The same values stored as [B, N, H, d], returned as a [B, H, N, d] view."""
+    return t.transpose(1, 2).contiguous().transpose(1, 2)
+
+
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
+@pytest.mark.parametrize("case", [(2, 3, 300, 333, 64, False, [333, 100]), (1, 2, 257, 257, 128, True, None)],
+                         ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else ""))
+def test_bwd_strided_matches_contiguous_bitwise(case, dtype):
+    # Q, K, V, O, dO read and dQ, dK, dV written in the [B, N, H, d] layout
+    # (osattn_bwd_strided) give the contiguous call's gradients bit for bit,
+    # and therefore pass the oracle gate too.
+    B, H, Nq, Nkv, d, causal, kl = case
+    stats, (dq1, dk1, dv1) = run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed=4000 + Nq + Nkv + d)
+    q, k, v = make_qkv(B, H, Nq, Nkv, d, dtype, seed=4000 + Nq + Nkv + d, q_std=1.5)
+    g = torch.Generator().manual_seed(4000 + Nq + Nkv + d + 1)
+    do = torch.randn(B, H, Nq, d, generator=g).to(dtype)
+    qd, kd, vd, dod = (_bnhd(t.to(DEV)) for t in (q, k, v, do))
+    assert not qd.is_contiguous()
+    kld = None if kl is None else torch.tensor(kl, dtype=torch.int32, device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = osattn.fwd(qd, kd, vd, scale=scale, causal=causal, key_len=kld)
+    o = _bnhd(o)
+    outs = [torch.full((B, n, H, d), float("nan"), dtype=dtype, device=DEV).transpose(1, 2)
+            for n in (Nq, Nkv, Nkv)]
+    osattn.bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, key_len=kld,
+               dq=outs[0], dk=outs[1], dv=outs[2])
+    assert osattn.get_device_status() == osattn.OK
+    torch.cuda.synchronize()
+    for a, b in zip((dq1, dk1, dv1), outs):
+        assert torch.equal(a.view(torch.int16), b.contiguous().view(torch.int16))
