@@ -68,7 +68,7 @@ struct BwdCfg {
   static constexpr uint32_t kColAcc1 = 256 + HD;       // dK
 };
 
-struct __align__(8) BwdBars {
+struct __align__(16) BwdBars {
   uint64_t fixed_full;            // the tile pair loaded once (K, V or Q, dO)
   uint64_t full[4], empty[4];     // ring stages
   uint64_t sd_full[2];            // MMA -> elementwise: half x of both score tiles is ready
@@ -77,8 +77,8 @@ struct __align__(8) BwdBars {
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  float lse2[4][kT];              // dK/dV kernel, per stage: LSE * log2(e) of the tile's queries
-  float dsum[4][kT];              //   and their D (+inf and 0 for rows past Nq)
+  alignas(16) float lse2[4][kT];  // dK/dV kernel, per stage: LSE * log2(e) of the tile's queries
+  alignas(16) float dsum[4][kT];  //   and their D (+inf and 0 for rows past Nq)
 };
 
 template <int HD>
@@ -199,11 +199,12 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O
 // first 32 columns of those halves: P^T over S^T's (dK/dV kernel only) and
 // dS over dP's.
 
-// Elementwise pass over one 64-column half: two chunks of 32.  `first` is
-// the index (query for dK/dV, key for dQ) of the half's column 0.
-template <bool kF16, bool kWriteP, typename Vis, typename Col>
+// Elementwise pass over one 64-column half: two chunks of 32.  vis(x)
+// tells whether column x of the half is visible to this thread's row;
+// col4(x, L2, D) gives LSE * log2(e) and D for columns x .. x + 3.
+template <bool kF16, bool kWriteP, typename Vis, typename Col4>
 __device__ __forceinline__ void bwd_half(uint32_t s_addr, uint32_t dp_addr, float c, Vis&& vis,
-                                         Col&& col) {
+                                         Col4&& col4) {
 #pragma unroll 1
   for (int ch = 0; ch < 2; ++ch) {
     uint32_t sv[32], dv[32];
@@ -214,18 +215,22 @@ __device__ __forceinline__ void bwd_half(uint32_t s_addr, uint32_t dp_addr, floa
     reg_fence32(dv);
     uint32_t pk[16], gk[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float pr[2], gr[2];
+    for (int g = 0; g < 8; ++g) {
+      float4 L2, D;
+      col4(ch * 32 + 4 * g, L2, D);
+      const float l2[4] = {L2.x, L2.y, L2.z, L2.w}, dd[4] = {D.x, D.y, D.z, D.w};
+      float pr[4], gr[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int x = ch * 32 + 2 * e + u;  // column within the half
-        float l2, dd;
-        col(x, l2, dd);
-        pr[u] = vis(x) ? ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), c, -l2)) : 0.f;
-        gr[u] = pr[u] * (__uint_as_float(dv[2 * e + u]) - dd);
+      for (int u = 0; u < 4; ++u) {
+        const int x = ch * 32 + 4 * g + u;  // column within the half
+        pr[u] = vis(x) ? ex2_approx(fmaf(__uint_as_float(sv[4 * g + u]), c, -l2[u])) : 0.f;
+        gr[u] = pr[u] * (__uint_as_float(dv[4 * g + u]) - dd[u]);
       }
-      if (kWriteP) pk[e] = pack2<kF16>(pr[0], pr[1]);
-      gk[e] = pack2<kF16>(gr[0], gr[1]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (kWriteP) pk[2 * g + e] = pack2<kF16>(pr[2 * e], pr[2 * e + 1]);
+        gk[2 * g + e] = pack2<kF16>(gr[2 * e], gr[2 * e + 1]);
+      }
     }
     if (kWriteP) tmem_st_32x32b_x16(s_addr + ch * 16, pk);
     tmem_st_32x32b_x16(dp_addr + ch * 16, gk);
@@ -298,24 +303,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       for (int it = 0; it < n_it; ++it) {
         const int s = it % C::kStages;
+        const int q0 = (it0 + it) * kT;
+        const long long rowbase = static_cast<long long>(bh) * p.Nq;
+        // LSE and D of the tile's queries: read before waiting for the
+        // stage, so their latency hides behind the wait.
+        float l2[kT / 32], dd[kT / 32];
+#pragma unroll
+        for (int r = 0; r < kT / 32; ++r) {
+          const int q = q0 + lane + 32 * r;
+          l2[r] = INFINITY;
+          dd[r] = 0.f;
+          if (q < p.Nq) {
+            const float L = p.LSE[rowbase + q];
+            l2[r] = (L == -INFINITY) ? INFINITY : L * kLog2e;
+            dd[r] = p.D[rowbase + q];
+          }
+        }
         bool ok = true;
         if (it >= C::kStages)
           ok = mbar_wait(&bars->empty[s], static_cast<uint32_t>(it / C::kStages - 1) & 1u, wc,
                          kSiteBwdLoad);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const int q0 = (it0 + it) * kT;
-        const long long rowbase = static_cast<long long>(bh) * p.Nq;
 #pragma unroll
         for (int r = 0; r < kT / 32; ++r) {
-          const int qq = lane + 32 * r, q = q0 + qq;
-          float l2 = INFINITY, dd = 0.f;
-          if (q < p.Nq) {
-            const float L = p.LSE[rowbase + q];
-            l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-            dd = p.D[rowbase + q];
-          }
-          bars->lse2[s][qq] = l2;
-          bars->dsum[s][qq] = dd;
+          bars->lse2[s][lane + 32 * r] = l2[r];
+          bars->dsum[s][lane + 32 * r] = dd[r];
         }
         __syncwarp();
         if (lane == 0) {
@@ -413,15 +425,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after_sync();
-        const float* l2 = bars->lse2[s] + 64 * x;
-        const float* dd = bars->dsum[s] + 64 * x;
+        const float4* l2 = reinterpret_cast<const float4*>(bars->lse2[s] + 64 * x);
+        const float4* dd = reinterpret_cast<const float4*>(bars->dsum[s] + 64 * x);
         const int qx = q0 + 64 * x;
         bwd_half<kF16, true>(
             lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
             [&](int col) { return row_live && (!p.causal || kabs <= qx + col); },
-            [&](int col, float& L2, float& D) {
-              L2 = l2[col];
-              D = dd[col];
+            [&](int col, float4& L2, float4& D) {
+              L2 = l2[col >> 2];
+              D = dd[col >> 2];
             });
         tmem_st_wait();
         tc_fence_before_sync();
@@ -611,9 +623,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_half<kF16, false>(
             lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
             [&](int col) { return kx + col < kv_len && (!p.causal || kx + col <= q); },
-            [&](int, float& L2, float& D) {
-              L2 = l2;
-              D = Dq;
+            [&](int, float4& L2, float4& D) {
+              L2 = make_float4(l2, l2, l2, l2);
+              D = make_float4(Dq, Dq, Dq, Dq);
             });
         tmem_st_wait();
         tc_fence_before_sync();
