@@ -17,7 +17,7 @@
 //                      shared memory while the query tiles that can see
 //                      those keys stream through a TMA ring.  Per query tile:
 //                        S^T  = K Q^T   and  dP^T = V dO^T   (tensor memory)
-//                        P^T, dS^T in 16-bit over the first halves of both
+//                        P^T, dS^T in 16-bit over the first 64 columns of each
 //                        dV += P^T dO   and  dK += dS^T Q     (A from tensor memory)
 //   bwd_dq_kernel      one CTA per 128-row query tile: Q and dO stay, the
 //                      visible K/V tiles stream.  Per key tile:
@@ -26,16 +26,17 @@
 // S and dP are computed twice (once per kernel) so that no kernel needs
 // atomics: each output element is written once, by one CTA.
 //
-// CTA layout (192 threads): warps 0-3 elementwise (one tile row per thread,
-// tensor-memory lane = row), warp 4 producer (TMA; its lanes stage LSE and
-// D of the dK/dV kernel's query tiles), warp 5 allocates tensor memory and
-// one of its threads issues the MMAs.  Every wait is bounded as in the
+// CTA layout (320 threads): warps 0-7 elementwise in two warpgroups, group g
+// taking columns 64g .. 64g + 63 of every score tile (one tile row per
+// thread, tensor-memory lane = row), warp 8 producer (TMA; its lanes stage
+// LSE and D of the dK/dV kernel's query tiles), warp 9 allocates tensor
+// memory and one of its threads issues the MMAs.  Every wait is bounded as in the
 // forward kernel: a wait past the limit records OSATTN_ERR_TIMEOUT, the CTA
 // drains its own copies and MMAs, frees tensor memory and returns.
 //
-// Tensor memory (512 columns): [0, 128) S or S^T, [128, 256) dP or dP^T
-// (each as two 64-column halves; P^T and dS are packed over the first 32
-// columns of their half), [256, 256 + d) dV or dQ, [256 + d, 256 + 2d) dK.
+// Tensor memory (512 columns), dK/dV kernel: [0, 128) S^T, [128, 256) dP^T,
+// [256, 256 + d) dV, [256 + d, 256 + 2d) dK.  dQ kernel: [0, 256) two S
+// buffers, [256, 384) dP, [384, 384 + d) dQ.
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -50,8 +51,8 @@ namespace osattn {
 namespace {
 
 constexpr int kT = 128;            // rows of every tile (keys or queries)
-constexpr int kBwdThreads = 192;   // warps 0-3 elementwise, 4 producer, 5 MMA
-constexpr int kProdWarp = 4, kMmaWarp = 5;
+constexpr int kBwdThreads = 320;   // warps 0-7 elementwise, 8 producer, 9 MMA
+constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -71,8 +72,11 @@ struct BwdCfg {
 struct __align__(16) BwdBars {
   uint64_t fixed_full;            // the tile pair loaded once (K, V or Q, dO)
   uint64_t full[4], empty[4];     // ring stages
-  uint64_t sd_full[2];            // MMA -> elementwise: half x of both score tiles is ready
-  uint64_t p_full[2];             // elementwise -> MMA: half x's 16-bit operands are written (128)
+  uint64_t s_full[2];             // MMA -> elementwise: a score tile (S or S^T) is ready
+                                  //   (the dQ kernel alternates two S buffers)
+  uint64_t dp_full;               // MMA -> elementwise: dP or dP^T is ready
+  uint64_t p_full;                // elementwise -> MMA: P^T written (dK/dV kernel; 256 arrivals)
+  uint64_t ds_full;               // elementwise -> MMA: dS or dS^T written (256 arrivals)
   uint64_t acc_full;              // MMA -> epilogue: the last accumulation is done
   uint64_t mma_drain;
   uint32_t tmem_base;
@@ -121,14 +125,14 @@ __device__ __forceinline__ int clamp_key_len(const int32_t* key_len, int b, int 
   return key_len ? min(max(key_len[b], 0), Nkv) : Nkv;
 }
 
-// Writes one 128-row tile row of `cols` fp32 tensor-memory columns starting
-// at col0, times `mul`, as 16-bit values to dst (or zeros when has_acc is
-// false).  The loads are warp-wide; only the stores depend on `store`.
-template <int HD, bool kF16>
+// Writes NC fp32 tensor-memory columns of one tile row, starting at taddr,
+// times `mul`, as 16-bit values to dst (or zeros when has_acc is false).
+// The loads are warp-wide; only the stores depend on `store`.
+template <int NC, bool kF16>
 __device__ __forceinline__ void write_row(uint16_t* dst, uint32_t taddr, bool has_acc, bool store,
                                           float mul) {
 #pragma unroll
-  for (int ch = 0; ch < HD / 32; ++ch) {
+  for (int ch = 0; ch < NC / 32; ++ch) {
     uint32_t r[32];
     if (has_acc) {
       tmem_ld_32x32b_x32(taddr + ch * 32, r);
@@ -190,51 +194,94 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O
   }
 }
 
-// Both kernels split every 128-column score tile into two 64-column halves
-// h = 0, 1 with their own barriers: while the elementwise warps turn half h
-// into 16-bit operands, the tensor core computes the other half or
-// accumulates the one finished before, so the MMAs of a tile overlap its
-// elementwise work.  Score half h sits at tensor-memory column 64h (S or
-// S^T) and 128 + 64h (dP or dP^T); the 16-bit results are written over the
-// first 32 columns of those halves: P^T over S^T's (dK/dV kernel only) and
-// dS over dP's.
+// Both kernels issue every score product at full width (128 x 128, N = 128
+// MMAs) and overlap it with the elementwise work in two parts per tile: the
+// P part (P = 2^{s * scale * log2(e) - LSE * log2(e)} on the visible
+// entries, kept in fp32 registers) needs only the scores, the dS part
+// (dS = P (dP - D), rounded to 16 bits) then waits for dP.  Warpgroup g
+// handles columns 64g .. 64g + 63 and writes its 16-bit results over the
+// first 32 of them (column pair (2e, 2e + 1) of the group in column e), so
+// the two groups never touch each other's columns; the MMAs that read those
+// results take 16-element steps 0-3 from columns 0-31 and 4-7 from 64-95.
 
-// Elementwise pass over one 64-column half: two chunks of 32.  vis(x)
-// tells whether column x of the half is visible to this thread's row;
-// col4(x, L2, D) gives LSE * log2(e) and D for columns x .. x + 3.
-template <bool kF16, bool kWriteP, typename Vis, typename Col4>
-__device__ __forceinline__ void bwd_half(uint32_t s_addr, uint32_t dp_addr, float c, Vis&& vis,
-                                         Col4&& col4) {
-#pragma unroll 1
+// P part over the 64 columns of this thread's group at tile column c0:
+// pr[x] = P of column c0 + x; kMask applies vis(column), l2of4(column)
+// gives LSE * log2(e) of 4 columns.  With kWriteP the 16-bit P is written
+// over columns c0 .. c0 + 31.
+template <bool kF16, bool kWriteP, bool kMask, typename Vis, typename L2of4>
+__device__ __forceinline__ void bwd_p_part(uint32_t s_addr, int c0, float c, Vis&& vis,
+                                           L2of4&& l2of4, float (&pr)[64]) {
+  uint32_t sa[32], sb[32];
+  tmem_ld_32x32b_x32(s_addr + c0, sa);
+  tmem_ld_32x32b_x32(s_addr + c0 + 32, sb);
+  tmem_ld_wait();
+  reg_fence32(sa);
+  reg_fence32(sb);
+#pragma unroll
+  for (int g = 0; g < 16; ++g) {
+    const float4 L = l2of4(c0 + 4 * g);
+    const float l2[4] = {L.x, L.y, L.z, L.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = 4 * g + u;
+      const uint32_t sv = g < 8 ? sa[x] : sb[x - 32];
+      const float e = ex2_approx(fmaf(__uint_as_float(sv), c, -l2[u]));
+      if constexpr (kMask) pr[x] = vis(c0 + x) ? e : 0.f;
+      else pr[x] = e;
+    }
+  }
+  if constexpr (kWriteP) {
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = pack2<kF16>(pr[32 * ch + 2 * e], pr[32 * ch + 2 * e + 1]);
+      tmem_st_32x32b_x16(s_addr + c0 + 16 * ch, pk);
+    }
+  }
+}
+
+// dS part over the same 64 columns of the dP tile at dp_addr, written as
+// 16-bit pairs over columns c0 .. c0 + 31; dof4(column) gives D of 4
+// columns.  Chunk ch reads columns c0 + 32ch .. + 31 and writes
+// c0 + 16ch .. + 15, which only earlier reads of this thread covered.
+template <bool kF16, typename Dof4>
+__device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& dof4,
+                                            const float (&pr)[64]) {
+#pragma unroll
   for (int ch = 0; ch < 2; ++ch) {
-    uint32_t sv[32], dv[32];
-    tmem_ld_32x32b_x32(s_addr + ch * 32, sv);
-    tmem_ld_32x32b_x32(dp_addr + ch * 32, dv);
+    uint32_t dv[32];
+    tmem_ld_32x32b_x32(dp_addr + c0 + 32 * ch, dv);
     tmem_ld_wait();
-    reg_fence32(sv);
     reg_fence32(dv);
-    uint32_t pk[16], gk[16];
+    uint32_t gk[16];
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-      float4 L2, D;
-      col4(ch * 32 + 4 * g, L2, D);
-      const float l2[4] = {L2.x, L2.y, L2.z, L2.w}, dd[4] = {D.x, D.y, D.z, D.w};
-      float pr[4], gr[4];
+      const float4 D = dof4(c0 + 32 * ch + 4 * g);
+      const float dd[4] = {D.x, D.y, D.z, D.w};
+      float gr[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int x = ch * 32 + 4 * g + u;  // column within the half
-        pr[u] = vis(x) ? ex2_approx(fmaf(__uint_as_float(sv[4 * g + u]), c, -l2[u])) : 0.f;
-        gr[u] = pr[u] * (__uint_as_float(dv[4 * g + u]) - dd[u]);
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (kWriteP) pk[2 * g + e] = pack2<kF16>(pr[2 * e], pr[2 * e + 1]);
-        gk[2 * g + e] = pack2<kF16>(gr[2 * e], gr[2 * e + 1]);
-      }
+      for (int u = 0; u < 4; ++u)
+        gr[u] = pr[32 * ch + 4 * g + u] * (__uint_as_float(dv[4 * g + u]) - dd[u]);
+      gk[2 * g] = pack2<kF16>(gr[0], gr[1]);
+      gk[2 * g + 1] = pack2<kF16>(gr[2], gr[3]);
     }
-    if (kWriteP) tmem_st_32x32b_x16(s_addr + ch * 16, pk);
-    tmem_st_32x32b_x16(dp_addr + ch * 16, gk);
+    tmem_st_32x32b_x16(dp_addr + c0 + 16 * ch, gk);
   }
+}
+
+// D (128 x N fp32) (+)= A B over 128 inner elements: A the 16-bit operand
+// the two warpgroups wrote (elements 0-63 in columns 0-31 of a_tmem,
+// 64-127 in 64-95), B an MN-major tile, 16 rows (2 KB) per MMA.
+template <int N, bool kF16>
+__device__ __forceinline__ void mma_tmem_a_groups(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  bool accumulate) {
+  constexpr uint32_t id = idesc_f16_f32(128, N, 1, kF16);  // B is MN-major
+  mma_bf16_ts(d_tmem, a_tmem, b_desc, id, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < 8; ++kk)
+    mma_ts_k<1>(d_tmem, a_tmem + (kk / 4) * 64 + (kk % 4) * 8,
+                sdesc_add(b_desc, static_cast<uint32_t>((kk * 2048) >> 4)), id);
 }
 
 // ------------------------------------------------------------------ dK, dV
@@ -270,10 +317,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars->sd_full[x], 1);
-      mbar_init(&bars->p_full[x], 128);
-    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
@@ -351,55 +399,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    // Order: S^T_0, dP^T_0, S^T_1, dP^T_1 of tile 0; then per tile it and
-    // half x: dV, dK += (half x of it), then S^T_x, dP^T_x of tile it + 1.
+    // Tensor memory: S^T at column 0 (P^T packed over its first 64 columns),
+    // dP^T at 128 (dS^T packed over its first 64), dV and dK after them.
+    // Order: S^T_0, dP^T_0; then per query tile it: dV += P^T_it dO_it,
+    // S^T_{it+1}, dK += dS^T_it Q_it, dP^T_{it+1}.  The tensor core runs
+    // them in issue order, so a product that overwrites a tile follows the
+    // one that reads it.
     if (lane == 0 && n_it > 0) {
       const uint64_t kA = sdesc_sw128(smem_u32(sK), 16, 1024);  // K-major A
       const uint64_t vA = sdesc_sw128(smem_u32(sV), 16, 1024);
-      constexpr uint32_t kHalfRows = 64 * 128 >> 4;             // 64 rows of a column block
       bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
       if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
       if (ok) {
         tc_fence_after_sync();
         const uint32_t sq = smem_u32(ring), sdo = sq + C::kTileBytes;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          mma_abt<64, HD, kF16>(tmem + 64 * x, kA, sdesc_add(sdesc_sw128(sq, 16, 1024), x * kHalfRows));
-          mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, vA,
-                                sdesc_add(sdesc_sw128(sdo, 16, 1024), x * kHalfRows));
-          mma_commit(&bars->sd_full[x]);
-        }
+        mma_abt<128, HD, kF16>(tmem, kA, sdesc_sw128(sq, 16, 1024));
+        mma_commit(&bars->s_full[0]);
+        mma_abt<128, HD, kF16>(tmem + 128, vA, sdesc_sw128(sdo, 16, 1024));
+        mma_commit(&bars->dp_full);
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::kStages, s1 = (it + 1) % C::kStages;
         const uint32_t sq = smem_u32(ring + s * C::kStageBytes), sdo = sq + C::kTileBytes;
         const uint32_t nq = smem_u32(ring + s1 * C::kStageBytes), ndo = nq + C::kTileBytes;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          ok = mbar_wait(&bars->p_full[x], static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        const bool more = it + 1 < n_it;
+        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // dV += P^T dO: B = dO read MN-major
+        mma_tmem_a_groups<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sdo, kT * 128, 1024), it > 0);
+        if (more) {
+          ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
+                         kSiteBwdMma);
           if (!ok) break;
           tc_fence_after_sync();
-          // dV += P^T dO and dK += dS^T Q over the 64 queries of half x: B
-          // read MN-major from those 64 rows of the tiles
-          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc0, tmem + 64 * x,
-                                  sdesc_add(sdesc_sw128(sdo, kT * 128, 1024), x * kHalfRows),
-                                  it > 0 || x > 0);
-          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc1, tmem + 128 + 64 * x,
-                                  sdesc_add(sdesc_sw128(sq, kT * 128, 1024), x * kHalfRows),
-                                  it > 0 || x > 0);
-          if (x == 1) mma_commit(&bars->empty[s]);
-          if (it + 1 < n_it) {
-            if (x == 0) {
-              ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
-                             kSiteBwdMma);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
-            mma_abt<64, HD, kF16>(tmem + 64 * x, kA, sdesc_add(sdesc_sw128(nq, 16, 1024), x * kHalfRows));
-            mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, vA,
-                                  sdesc_add(sdesc_sw128(ndo, 16, 1024), x * kHalfRows));
-            mma_commit(&bars->sd_full[x]);
-          }
+          mma_abt<128, HD, kF16>(tmem, kA, sdesc_sw128(nq, 16, 1024));
+          mma_commit(&bars->s_full[0]);
+        }
+        ok = mbar_wait(&bars->ds_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // dK += dS^T Q: B = Q read MN-major
+        mma_tmem_a_groups<HD, kF16>(tmem + C::kColAcc1, tmem + 128, sdesc_sw128(sq, kT * 128, 1024),
+                                    it > 0);
+        mma_commit(&bars->empty[s]);
+        if (more) {
+          mma_abt<128, HD, kF16>(tmem + 128, vA, sdesc_sw128(ndo, 16, 1024));
+          mma_commit(&bars->dp_full);
         }
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -409,38 +455,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- elementwise
-    const int row = warp * 32 + lane;  // key row of the tile = tensor-memory lane
+    const int c0 = 64 * (warp >> 2);  // this warpgroup's columns (queries) of each tile
+    const int row = (warp & 3) * 32 + lane;  // key row of the tile = tensor-memory lane
     const int kabs = k0 + row;
     const bool row_live = kabs < kv_len;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it % C::kStages;
       const int q0 = (it0 + it) * kT;
-      for (int x = 0; x < 2; ++x) {
-        ok = mbar_wait(&bars->sd_full[x], static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
-        // LSE and D of this query tile were staged with the stage's loads.
-        if (ok && x == 0)
-          ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdElem);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const float4* l2 = reinterpret_cast<const float4*>(bars->lse2[s] + 64 * x);
-        const float4* dd = reinterpret_cast<const float4*>(bars->dsum[s] + 64 * x);
-        const int qx = q0 + 64 * x;
-        bwd_half<kF16, true>(
-            lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
-            [&](int col) { return row_live && (!p.causal || kabs <= qx + col); },
-            [&](int col, float4& L2, float4& D) {
-              L2 = l2[col >> 2];
-              D = dd[col >> 2];
-            });
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&bars->p_full[x]);
-      }
+      ok = mbar_wait(&bars->s_full[0], static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
+      // LSE and D of this query tile were staged with the stage's loads.
+      if (ok)
+        ok = mbar_wait(&bars->full[s], static_cast<uint32_t>(it / C::kStages) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const float4* l2 = reinterpret_cast<const float4*>(bars->lse2[s]);
+      const float4* dd = reinterpret_cast<const float4*>(bars->dsum[s]);
+      auto vis = [&](int col) { return row_live && (!p.causal || kabs <= q0 + col); };
+      auto l2of4 = [&](int col) { return l2[col >> 2]; };
+      float pr[64];
+      // No mask when every column of the group is visible to every row of
+      // the warp.  The branch must be warp-uniform: the tensor-memory loads
+      // inside are warp-collective.
+      if (__all_sync(0xffffffffu, row_live && (!p.causal || kabs <= q0 + c0)))
+        bwd_p_part<kF16, true, false>(lane_base, c0, p.scale_log2, vis, l2of4, pr);
+      else
+        bwd_p_part<kF16, true, true>(lane_base, c0, p.scale_log2, vis, l2of4, pr);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full);
+      ok = mbar_wait(&bars->dp_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      bwd_ds_part<kF16>(lane_base + 128, c0, [&](int col) { return dd[col >> 2]; }, pr);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->ds_full);
     }
-    // epilogue: dV = sum P^T dO, dK = scale * sum dS^T Q
+    // epilogue: warpgroup 0 writes dV = sum P^T dO, warpgroup 1 dK = scale * sum dS^T Q
     bool has_acc = false;
     if (ok && n_it > 0) {
       ok = mbar_wait(&bars->acc_full, 0, wc, kSiteBwdEpi);
@@ -450,10 +505,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       const bool store = kabs < p.Nkv;
-      write_row<HD, kF16>(p.dV + b * p.dv_s[0] + h * p.dv_s[1] + kabs * p.dv_s[2],
-                          lane_base + C::kColAcc0, has_acc, store, 1.f);
-      write_row<HD, kF16>(p.dK + b * p.dk_s[0] + h * p.dk_s[1] + kabs * p.dk_s[2],
-                          lane_base + C::kColAcc1, has_acc, store, p.scale);
+      if (c0 == 0)
+        write_row<HD, kF16>(p.dV + b * p.dv_s[0] + h * p.dv_s[1] + kabs * p.dv_s[2],
+                            lane_base + C::kColAcc0, has_acc, store, 1.f);
+      else
+        write_row<HD, kF16>(p.dK + b * p.dk_s[0] + h * p.dk_s[1] + kabs * p.dk_s[2],
+                            lane_base + C::kColAcc1, has_acc, store, p.scale);
     }
   }
 
@@ -469,6 +526,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ
+// Tensor memory: S in two 128-column buffers (S_j at 128 (j mod 2)), dP at
+// 256 (dS packed over its first 64 columns), dQ at 384.
+constexpr uint32_t kDqColDP = 256, kDqColAcc = 384;
+
 template <int HD, bool kF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -500,10 +561,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars->sd_full[x], 1);
-      mbar_init(&bars->p_full[x], 128);
-    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_drain, 1);
     bars->abort_flag = 0;
@@ -548,52 +610,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         drain(&bars->full[j % C::kStages], static_cast<uint32_t>(j / C::kStages) & 1u, wc.limit_ns);
     }
   } else if (warp == kMmaWarp) {
-    // Order: S_0, dP_0, S_1, dP_1 of key tile 0; then per key tile j and
-    // half x: dQ += dS_x K_x, then S_x, dP_x of key tile j + 1.
+    // Order: S_0, dP_0; then per key tile j: S_{j+1} (other S buffer),
+    // dQ += dS_j K_j, dP_{j+1}.  S_{j+1} overwrites S_{j-1}, whose reader
+    // signalled ds_full for tile j - 1 before the previous dQ product.
     if (lane == 0 && n_kt > 0) {
       const uint64_t qA = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dA = sdesc_sw128(smem_u32(sdO), 16, 1024);
-      constexpr uint32_t kHalfRows = 64 * 128 >> 4;
       bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
       if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
       if (ok) {
         tc_fence_after_sync();
         const uint32_t sk = smem_u32(ring), sv = sk + C::kTileBytes;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          mma_abt<64, HD, kF16>(tmem + 64 * x, qA, sdesc_add(sdesc_sw128(sk, 16, 1024), x * kHalfRows));
-          mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, dA,
-                                sdesc_add(sdesc_sw128(sv, 16, 1024), x * kHalfRows));
-          mma_commit(&bars->sd_full[x]);
-        }
+        mma_abt<128, HD, kF16>(tmem, qA, sdesc_sw128(sk, 16, 1024));
+        mma_commit(&bars->s_full[0]);
+        mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(sv, 16, 1024));
+        mma_commit(&bars->dp_full);
       }
       for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
         const uint32_t sk = smem_u32(ring + s * C::kStageBytes);
         const uint32_t nk = smem_u32(ring + s1 * C::kStageBytes), nv = nk + C::kTileBytes;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          ok = mbar_wait(&bars->p_full[x], static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
+        const bool more = j + 1 < n_kt;
+        if (more) {
+          ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((j + 1) / C::kStages) & 1u, wc,
+                         kSiteBwdMma);
           if (!ok) break;
           tc_fence_after_sync();
-          // dQ += dS K over the 64 keys of half x (dS over dP's half): K read
-          // MN-major from those keys
-          mma_tmem_a<HD, 4, kF16>(tmem + C::kColAcc0, tmem + 128 + 64 * x,
-                                  sdesc_add(sdesc_sw128(sk, kT * 128, 1024), x * kHalfRows),
-                                  j > 0 || x > 0);
-          if (x == 1) mma_commit(&bars->empty[s]);
-          if (j + 1 < n_kt) {
-            if (x == 0) {
-              ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((j + 1) / C::kStages) & 1u, wc,
-                             kSiteBwdMma);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
-            mma_abt<64, HD, kF16>(tmem + 64 * x, qA, sdesc_add(sdesc_sw128(nk, 16, 1024), x * kHalfRows));
-            mma_abt<64, HD, kF16>(tmem + 128 + 64 * x, dA,
-                                  sdesc_add(sdesc_sw128(nv, 16, 1024), x * kHalfRows));
-            mma_commit(&bars->sd_full[x]);
-          }
+          mma_abt<128, HD, kF16>(tmem + 128 * ((j + 1) & 1), qA, sdesc_sw128(nk, 16, 1024));
+          mma_commit(&bars->s_full[(j + 1) & 1]);
+        }
+        ok = mbar_wait(&bars->ds_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
+        if (!ok) break;
+        tc_fence_after_sync();
+        // dQ += dS K: B = K_j read MN-major
+        mma_tmem_a_groups<HD, kF16>(tmem + kDqColAcc, tmem + kDqColDP,
+                                    sdesc_sw128(sk, kT * 128, 1024), j > 0);
+        mma_commit(&bars->empty[s]);
+        if (more) {
+          mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(nv, 16, 1024));
+          mma_commit(&bars->dp_full);
         }
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -601,7 +656,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       drain(&bars->mma_drain, 0, wc.limit_ns);
     }
   } else {
-    const int row = warp * 32 + lane;  // query row of the tile = tensor-memory lane
+    const int c0 = 64 * (warp >> 2);  // this warpgroup's columns (keys) of each tile
+    const int row = (warp & 3) * 32 + lane;  // query row of the tile = tensor-memory lane
     const int q = q0 + row;
     const bool row_live = q < p.Nq;
     const long long rix = static_cast<long long>(bh) * p.Nq + q;
@@ -611,26 +667,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
       Dq = p.D[rix];
     }
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float4 l2v = make_float4(l2, l2, l2, l2), dv4 = make_float4(Dq, Dq, Dq, Dq);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     bool ok = true;
     for (int j = 0; ok && j < n_kt; ++j) {
-      for (int x = 0; x < 2; ++x) {
-        ok = mbar_wait(&bars->sd_full[x], static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const int kx = j * kT + 64 * x;
-        bwd_half<kF16, false>(
-            lane_base + 64 * x, lane_base + 128 + 64 * x, p.scale_log2,
-            [&](int col) { return kx + col < kv_len && (!p.causal || kx + col <= q); },
-            [&](int, float4& L2, float4& D) {
-              L2 = make_float4(l2, l2, l2, l2);
-              D = make_float4(Dq, Dq, Dq, Dq);
-            });
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&bars->p_full[x]);
-      }
+      ok = mbar_wait(&bars->s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int kx = j * kT;
+      auto vis = [&](int col) { return kx + col < kv_len && (!p.causal || kx + col <= q); };
+      auto l2of4 = [&](int) { return l2v; };
+      const int last = kx + c0 + 63;  // the group's last key
+      float pr[64];
+      // No mask when every key of the group is visible to every row of the
+      // warp (a warp-uniform branch: the tensor-memory loads inside are
+      // warp-collective).
+      if (__all_sync(0xffffffffu, last < kv_len && (!p.causal || last <= q)))
+        bwd_p_part<kF16, false, false>(lane_base + 128 * (j & 1), c0, p.scale_log2, vis, l2of4, pr);
+      else
+        bwd_p_part<kF16, false, true>(lane_base + 128 * (j & 1), c0, p.scale_log2, vis, l2of4, pr);
+      ok = mbar_wait(&bars->dp_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      bwd_ds_part<kF16>(lane_base + kDqColDP, c0, [&](int) { return dv4; }, pr);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->ds_full);
     }
     bool has_acc = false;
     if (ok && n_kt > 0) {
@@ -639,9 +703,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) tc_fence_after_sync();
       has_acc = ok;
     }
+    // warpgroup g writes dQ columns g * d/2 .. (g + 1) * d/2 - 1
     if (ok)
-      write_row<HD, kF16>(p.dQ + b * p.dq_s[0] + h * p.dq_s[1] + q * p.dq_s[2],
-                          lane_base + C::kColAcc0, has_acc, row_live, p.scale);
+      write_row<HD / 2, kF16>(p.dQ + b * p.dq_s[0] + h * p.dq_s[1] + q * p.dq_s[2] + c0 * HD / 128,
+                              lane_base + kDqColAcc + c0 * HD / 128, has_acc, row_live, p.scale);
   }
 
   __syncwarp();
