@@ -62,16 +62,26 @@ enum : uint32_t { kSiteBwdLoad = 21, kSiteBwdMma = 22, kSiteBwdElem = 23, kSiteB
 template <int HD>
 struct BwdCfg {
   static constexpr int kTileBytes = kT * HD * 2;       // one 128-row tile
-  static constexpr int kStages = HD == 128 ? 2 : 4;    // ring stages, two tiles each
+  // dK/dV kernel: K, V, then kStages stages of (Q_i, dO_i), then LSE and D
+  // of each stage's queries.
+  static constexpr int kStages = HD == 128 ? 2 : 4;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kRegion = 2 * kTileBytes + kStages * kStageBytes;  // fixed pair + ring
-  static constexpr uint32_t kColAcc0 = 256;            // dV or dQ
+  static constexpr int kDkdvLse = 2 * kTileBytes + kStages * kStageBytes;
+  static constexpr int kDkdvRegion = kDkdvLse + 2 * kStages * kT * 4;
+  // dQ kernel: Q, dO, then kKSlots K tiles and kVSlots V tiles (K_j is read
+  // until dQ_j, V_j only until dP_j, so K needs the deeper ring).
+  static constexpr int kKSlots = HD == 128 ? 3 : 4;
+  static constexpr int kVSlots = HD == 128 ? 2 : 4;
+  static constexpr int kDqRegion = (2 + kKSlots + kVSlots) * kTileBytes;
+  static constexpr uint32_t kColAcc0 = 256;            // dV
   static constexpr uint32_t kColAcc1 = 256 + HD;       // dK
 };
 
 struct __align__(16) BwdBars {
   uint64_t fixed_full;            // the tile pair loaded once (K, V or Q, dO)
-  uint64_t full[4], empty[4];     // ring stages
+  uint64_t full[4];               // per ring tile: its loads landed (dK/dV: and LSE, D staged)
+  uint64_t empty[4];              // dK/dV: Q slot free (after dK); dQ: K slot free (after dQ)
+  uint64_t empty2[4];             // dK/dV: dO slot free (after dV); dQ: V slot free (after dP)
   uint64_t s_full[2];             // MMA -> elementwise: a score tile (S or S^T) is ready
                                   //   (the dQ kernel alternates two S buffers)
   uint64_t dp_full;               // MMA -> elementwise: dP or dP^T is ready
@@ -81,14 +91,19 @@ struct __align__(16) BwdBars {
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) float lse2[4][kT];  // dK/dV kernel, per stage: LSE * log2(e) of the tile's queries
-  alignas(16) float dsum[4][kT];  //   and their D (+inf and 0 for rows past Nq)
 };
 
 template <int HD>
-constexpr int bwd_smem_bytes() {
-  return BwdCfg<HD>::kRegion + static_cast<int>(sizeof(BwdBars)) + 1024;
+constexpr int dkdv_smem_bytes() {
+  return BwdCfg<HD>::kDkdvRegion + static_cast<int>(sizeof(BwdBars)) + 1024;
 }
+template <int HD>
+constexpr int dq_smem_bytes() {
+  return BwdCfg<HD>::kDqRegion + static_cast<int>(sizeof(BwdBars)) + 1024;
+}
+static_assert(dkdv_smem_bytes<128>() <= 232448 && dq_smem_bytes<128>() <= 232448 &&
+                  dkdv_smem_bytes<64>() <= 232448 && dq_smem_bytes<64>() <= 232448,
+              "shared memory per CTA");
 
 struct BwdParams {
   uint16_t* dQ;
@@ -119,6 +134,14 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity, uint64_t l
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > limit_ns) return;
   }
+}
+
+// Counts tx_bytes of an mbarrier's expected transaction bytes as arrived
+// (for a copy that will not be issued after all).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t tx_bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(tx_bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ int clamp_key_len(const int32_t* key_len, int b, int Nkv) {
@@ -297,7 +320,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kTileBytes;
   uint8_t* ring = smem + 2 * C::kTileBytes;  // stage s: Q_i at +0, dO_i at +kTileBytes
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kRegion);
+  float* lse2 = reinterpret_cast<float*>(smem + C::kDkdvLse);  // [stage][query]: LSE * log2(e)
+  float* dsum = lse2 + C::kStages * kT;                        //   and D (+inf, 0 past Nq)
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kDkdvRegion);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int bh = blockIdx.x / p.num_tiles;
@@ -314,8 +339,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->fixed_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->full[s], 2);  // the dO load's expect-tx, then the Q load's arrival
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->empty2[s], 1);
     }
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
@@ -367,27 +393,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dd[r] = p.D[rowbase + q];
           }
         }
+        uint8_t* st = ring + s * C::kStageBytes;
+        // dO_i's slot frees after dV of the tile before (half a tile before
+        // Q_i's, which frees after dK): load it first.
         bool ok = true;
+        if (it >= C::kStages)
+          ok = mbar_wait(&bars->empty2[s], static_cast<uint32_t>(it / C::kStages - 1) & 1u, wc,
+                         kSiteBwdLoad);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->full[s], 2 * C::kTileBytes);
+#pragma unroll
+          for (int cb = 0; cb < HD / 64; ++cb)
+            tma_load_4d(st + C::kTileBytes + cb * kT * 128, &tmdO, &bars->full[s], cb * 64, q0, h, b);
+        }
+        issued = it + 1;  // dO_i is in flight: the drain below must cover this tile
         if (it >= C::kStages)
           ok = mbar_wait(&bars->empty[s], static_cast<uint32_t>(it / C::kStages - 1) & 1u, wc,
                          kSiteBwdLoad);
-        if (!__all_sync(0xffffffffu, ok)) break;
+        if (!__all_sync(0xffffffffu, ok)) {
+          // Q_i will not be loaded: count its bytes and arrival as done, so
+          // the phase completes once dO_i has landed.
+          if (lane == 0) {
+            mbar_complete_tx(&bars->full[s], C::kTileBytes);
+            mbar_arrive(&bars->full[s]);
+          }
+          break;
+        }
 #pragma unroll
         for (int r = 0; r < kT / 32; ++r) {
-          bars->lse2[s][lane + 32 * r] = l2[r];
-          bars->dsum[s][lane + 32 * r] = dd[r];
+          lse2[s * kT + lane + 32 * r] = l2[r];
+          dsum[s * kT + lane + 32 * r] = dd[r];
         }
         __syncwarp();
         if (lane == 0) {
-          uint8_t* st = ring + s * C::kStageBytes;
-          mbar_arrive_expect_tx(&bars->full[s], 2 * C::kTileBytes);
 #pragma unroll
-          for (int cb = 0; cb < HD / 64; ++cb) {
+          for (int cb = 0; cb < HD / 64; ++cb)
             tma_load_4d(st + cb * kT * 128, &tmQ, &bars->full[s], cb * 64, q0, h, b);
-            tma_load_4d(st + C::kTileBytes + cb * kT * 128, &tmdO, &bars->full[s], cb * 64, q0, h, b);
-          }
+          mbar_arrive(&bars->full[s]);  // releases the LSE and D writes above
         }
-        issued = it + 1;
       }
       // Let every load of this CTA land before it can exit.
       if (lane == 0) {
@@ -428,6 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after_sync();
         // dV += P^T dO: B = dO read MN-major
         mma_tmem_a_groups<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sdo, kT * 128, 1024), it > 0);
+        mma_commit(&bars->empty2[s]);
         if (more) {
           ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
                          kSiteBwdMma);
@@ -471,8 +516,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      const float4* l2 = reinterpret_cast<const float4*>(bars->lse2[s]);
-      const float4* dd = reinterpret_cast<const float4*>(bars->dsum[s]);
+      const float4* l2 = reinterpret_cast<const float4*>(lse2 + s * kT);
+      const float4* dd = reinterpret_cast<const float4*>(dsum + s * kT);
       auto vis = [&](int col) { return row_live && (!p.causal || kabs <= q0 + col); };
       auto l2of4 = [&](int col) { return l2[col >> 2]; };
       float pr[64];
@@ -541,8 +586,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sdO = smem + C::kTileBytes;
-  uint8_t* ring = smem + 2 * C::kTileBytes;  // stage s: K_j at +0, V_j at +kTileBytes
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kRegion);
+  uint8_t* kring = smem + 2 * C::kTileBytes;            // K_j in slot j mod kKSlots
+  uint8_t* vring = kring + C::kKSlots * C::kTileBytes;  // V_j in slot j mod kVSlots
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kDqRegion);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int bh = blockIdx.x / p.num_tiles;
@@ -557,10 +603,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->fixed_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKSlots; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
+    for (int s = 0; s < C::kVSlots; ++s) mbar_init(&bars->empty2[s], 1);
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->dp_full, 1);
@@ -589,25 +636,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sQ + cb * kT * 128, &tmQ, &bars->fixed_full, cb * 64, q0, h, b);
         tma_load_4d(sdO + cb * kT * 128, &tmdO, &bars->fixed_full, cb * 64, q0, h, b);
       }
+      // Tile j: K_j and V_j on full[j mod kKSlots], once both slots are free.
       int issued = 0;
       for (int j = 0; j < n_kt; ++j) {
-        const int s = j % C::kStages;
-        if (j >= C::kStages &&
-            !mbar_wait(&bars->empty[s], static_cast<uint32_t>(j / C::kStages - 1) & 1u, wc,
+        const int a = j % C::kKSlots, v = j % C::kVSlots;
+        if (j >= C::kKSlots &&
+            !mbar_wait(&bars->empty[a], static_cast<uint32_t>(j / C::kKSlots - 1) & 1u, wc,
                        kSiteBwdLoad))
           break;
-        uint8_t* st = ring + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&bars->full[s], 2 * C::kTileBytes);
+        if (j >= C::kVSlots &&
+            !mbar_wait(&bars->empty2[v], static_cast<uint32_t>(j / C::kVSlots - 1) & 1u, wc,
+                       kSiteBwdLoad))
+          break;
+        mbar_arrive_expect_tx(&bars->full[a], 2 * C::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb) {
-          tma_load_4d(st + cb * kT * 128, &tmK, &bars->full[s], cb * 64, j * kT, h, b);
-          tma_load_4d(st + C::kTileBytes + cb * kT * 128, &tmV, &bars->full[s], cb * 64, j * kT, h, b);
+          tma_load_4d(kring + a * C::kTileBytes + cb * kT * 128, &tmK, &bars->full[a], cb * 64, j * kT,
+                      h, b);
+          tma_load_4d(vring + v * C::kTileBytes + cb * kT * 128, &tmV, &bars->full[a], cb * 64, j * kT,
+                      h, b);
         }
         issued = j + 1;
       }
       drain(&bars->fixed_full, 0, wc.limit_ns);
-      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
-        drain(&bars->full[j % C::kStages], static_cast<uint32_t>(j / C::kStages) & 1u, wc.limit_ns);
+      for (int j = (issued > C::kKSlots ? issued - C::kKSlots : 0); j < issued; ++j)
+        drain(&bars->full[j % C::kKSlots], static_cast<uint32_t>(j / C::kKSlots) & 1u, wc.limit_ns);
     }
   } else if (warp == kMmaWarp) {
     // Order: S_0, dP_0; then per key tile j: S_{j+1} (other S buffer),
@@ -620,19 +673,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
       if (ok) {
         tc_fence_after_sync();
-        const uint32_t sk = smem_u32(ring), sv = sk + C::kTileBytes;
-        mma_abt<128, HD, kF16>(tmem, qA, sdesc_sw128(sk, 16, 1024));
+        mma_abt<128, HD, kF16>(tmem, qA, sdesc_sw128(smem_u32(kring), 16, 1024));
         mma_commit(&bars->s_full[0]);
-        mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(sv, 16, 1024));
+        mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(smem_u32(vring), 16, 1024));
         mma_commit(&bars->dp_full);
+        mma_commit(&bars->empty2[0]);
       }
       for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
-        const uint32_t sk = smem_u32(ring + s * C::kStageBytes);
-        const uint32_t nk = smem_u32(ring + s1 * C::kStageBytes), nv = nk + C::kTileBytes;
+        const int a = j % C::kKSlots, a1 = (j + 1) % C::kKSlots, v1 = (j + 1) % C::kVSlots;
+        const uint32_t sk = smem_u32(kring + a * C::kTileBytes);
+        const uint32_t nk = smem_u32(kring + a1 * C::kTileBytes);
+        const uint32_t nv = smem_u32(vring + v1 * C::kTileBytes);
         const bool more = j + 1 < n_kt;
         if (more) {
-          ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((j + 1) / C::kStages) & 1u, wc,
+          ok = mbar_wait(&bars->full[a1], static_cast<uint32_t>((j + 1) / C::kKSlots) & 1u, wc,
                          kSiteBwdMma);
           if (!ok) break;
           tc_fence_after_sync();
@@ -645,10 +699,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dQ += dS K: B = K_j read MN-major
         mma_tmem_a_groups<HD, kF16>(tmem + kDqColAcc, tmem + kDqColDP,
                                     sdesc_sw128(sk, kT * 128, 1024), j > 0);
-        mma_commit(&bars->empty[s]);
+        mma_commit(&bars->empty[a]);
         if (more) {
           mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(nv, 16, 1024));
           mma_commit(&bars->dp_full);
+          mma_commit(&bars->empty2[v1]);
         }
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -723,10 +778,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int HD, bool kF16>
 cudaError_t set_bwd_attrs() {
   cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<HD, kF16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_smem_bytes<HD>());
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dkdv_smem_bytes<HD>());
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(bwd_dq_kernel<HD, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bwd_smem_bytes<HD>());
+                              dq_smem_bytes<HD>());
 }
 
 template <int HD, bool kF16>
@@ -753,11 +808,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
   pq.num_tiles = (a.Nq + kT - 1) / kT;
   const long long gq = static_cast<long long>(pq.num_tiles) * a.B * a.H;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
-  bwd_dkdv_kernel<HD, kF16><<<static_cast<unsigned>(gk), kBwdThreads, bwd_smem_bytes<HD>(), a.stream>>>(
+  bwd_dkdv_kernel<HD, kF16><<<static_cast<unsigned>(gk), kBwdThreads, dkdv_smem_bytes<HD>(), a.stream>>>(
       tmQ, tmK, tmV, tmdO, pk);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<HD, kF16><<<static_cast<unsigned>(gq), kBwdThreads, bwd_smem_bytes<HD>(), a.stream>>>(
+  bwd_dq_kernel<HD, kF16><<<static_cast<unsigned>(gq), kBwdThreads, dq_smem_bytes<HD>(), a.stream>>>(
       tmQ, tmK, tmV, tmdO, pq);
   return cudaGetLastError();
 }
