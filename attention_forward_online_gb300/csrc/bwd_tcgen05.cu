@@ -188,6 +188,10 @@ template <>
 __device__ __forceinline__ float2 load2<__half>(const __half* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
+template <>
+__device__ __forceinline__ float2 load2<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
 
 struct RowStrides {
   long long o[3], g[3];  // element strides of the b, h and row axes of O and dO
@@ -784,13 +788,12 @@ cudaError_t set_bwd_attrs() {
                               dq_smem_bytes<HD>());
 }
 
-template <int HD, bool kF16>
-cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensorMap& tmQ,
-                         const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO) {
+// D = rowsum(dO * O) into a.D, for element type T.
+template <typename T>
+cudaError_t launch_rowdot(const BwdArgs& a) {
   const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
   const long long want = static_cast<long long>(a.num_sms) * 16;
   const int rgrid = static_cast<int>((rows + 7) / 8 < want ? (rows + 7) / 8 : want);
-  using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
   RowStrides rs;
   for (int i = 0; i < 3; ++i) {
     rs.o[i] = a.o_strides[i];
@@ -799,7 +802,14 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
   bwd_rowdot_kernel<T><<<rgrid, 256, 0, a.stream>>>(static_cast<const T*>(a.O),
                                                     static_cast<const T*>(a.dO), a.D, rows, a.d,
                                                     a.H, a.Nq, rs);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int HD, bool kF16>
+cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensorMap& tmQ,
+                         const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO) {
+  using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
+  cudaError_t e = launch_rowdot<T>(a);
   if (e != cudaSuccess) return e;
   BwdParams pk = base;
   pk.num_tiles = (a.Nkv + kT - 1) / kT;
@@ -818,6 +828,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
 }
 
 }  // namespace
+
+cudaError_t launch_bwd_rowdot_fp32(const BwdArgs& a) { return launch_rowdot<float>(a); }
 
 cudaError_t prepare_bwd() {
   cudaError_t e;

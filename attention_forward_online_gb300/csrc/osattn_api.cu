@@ -56,7 +56,8 @@ int device_state(DeviceState** out) {
         cudaSuccess)
       return OSATTN_ERR_CUDA;
     if (osattn::prepare_fwd_bf16() != cudaSuccess) return OSATTN_ERR_CUDA;
-    if (osattn::prepare_bwd() != cudaSuccess) return OSATTN_ERR_CUDA;
+    if (osattn::prepare_bwd() != cudaSuccess || osattn::prepare_bwd_fp32() != cudaSuccess)
+      return OSATTN_ERR_CUDA;
     if (!g_encode_tiled) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -320,7 +321,6 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
   if (!dO || !dQ || !dK || !dV || !aligned(dO, 16) || !aligned(dQ, 16) || !aligned(dK, 16) ||
       !aligned(dV, 16))
     return OSATTN_ERR_INVALID_ARG;
-  if (dtype == OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < osattn_bwd_workspace_bytes(B, H, Nq))
     return OSATTN_ERR_INVALID_ARG;
@@ -361,6 +361,8 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
                        a.dq_strides, a.dk_strides, a.dv_strides};
   for (int i = 0; i < 8; ++i)
     for (int j = 0; j < 3; ++j) dst[i][j] = st[i][j];
+  if (dtype == OSATTN_FP32)
+    return osattn::launch_bwd_fp32(a) == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
   CUtensorMap tmQ, tmK, tmV, tmdO;
   if (encode_map(&tmQ, Q, a.fp16, d, Nq, H, B, st[0]) != OSATTN_OK ||
       encode_map(&tmK, K, a.fp16, d, Nkv, H, B, st[1]) != OSATTN_OK ||

@@ -81,6 +81,10 @@ struct BwdArgs {
 cudaError_t prepare_bwd();  // once per device: kernel attributes
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const CUtensorMap& tmdO);
+// fp32 path (bwd_fp32_simt.cu): D, then the SIMT dK/dV and dQ kernels.
+cudaError_t prepare_bwd_fp32();  // once per device: kernel attributes
+cudaError_t launch_bwd_fp32(const BwdArgs& a);
+cudaError_t launch_bwd_rowdot_fp32(const BwdArgs& a);  // D for fp32 O and dO (bwd_tcgen05.cu)
 
 // Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix;
 // elem: 0 bf16, 1 fp32, 2 fp16 (the public dtype codes).

@@ -258,7 +258,7 @@ def bwd(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False, k
         dq=None, dk=None, dv=None, workspace=None, stream=None):
     """dQ, dK, dV of the attention forward for the upstream gradient `do`.
 
-    q, k, v, o, do: CUDA bf16 or fp16 tensors ([B,H,Nq,d] for q, o, do;
+    q, k, v, o, do: CUDA bf16, fp16 or fp32 tensors ([B,H,Nq,d] for q, o, do;
     [B,H,Nkv,d] for k, v), any views whose last axis is contiguous; lse: the
     contiguous fp32 [B,H,Nq] LSE that fwd() returned for the same inputs.
     Contiguous tensors go through osattn_bwd, others through
@@ -269,8 +269,6 @@ def bwd(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False, k
 
     B, H, Nq, Nkv, d = _shapes(q, k, v)
     dtype = _dtype_code(q)
-    if dtype == FP32:
-        raise TypeError("the backward pass takes bf16 or fp16 tensors")
     for t in (o, do):
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda:
             raise ValueError("o and do must be CUDA tensors shaped and typed like q")

@@ -217,7 +217,9 @@ size_t osattn_bwd_workspace_bytes(int B, int H, int Nq);
  *   dQ        device, [B, H, Nq, d] contiguous, element type `dtype` (written)
  *   dK, dV    device, [B, H, Nkv, d] contiguous, element type `dtype` (written)
  *   B .. key_len   as for osattn_fwd
- *   dtype     OSATTN_BF16 or OSATTN_FP16 (OSATTN_FP32 -> OSATTN_ERR_UNSUPPORTED)
+ *   dtype     OSATTN_BF16, OSATTN_FP16 (tensor cores: P and dS rounded to the
+ *             input type for the products, fp32 accumulation) or OSATTN_FP32
+ *             (SIMT FMAs and expf throughout, for the fp32 forward)
  *   workspace caller-owned device memory, 16-byte aligned, at least
  *             osattn_bwd_workspace_bytes(B, H, Nq) bytes (else
  *             OSATTN_ERR_INVALID_ARG); overwritten, free once the stream
@@ -225,8 +227,8 @@ size_t osattn_bwd_workspace_bytes(int B, int H, int Nq);
  *
  * dO, dQ, dK, dV must be 16-byte aligned and must not overlap each other or
  * the inputs.  Three kernels are enqueued on `stream` (D, then dK/dV, then
- * dQ); each output element is written by one CTA, so the results do not
- * depend on scheduling.  The call allocates nothing.  Errors as for
+ * dQ); each output element is written by one CTA (one thread for fp32), so
+ * the results do not depend on scheduling.  The call allocates nothing.  Errors as for
  * osattn_fwd.
  */
 int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,

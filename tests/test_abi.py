@@ -221,8 +221,10 @@ def test_bwd_workspace_size(L):
     (dict(ws_bytes=8 * 4 - 1), osattn.ERR_INVALID_ARG),
     (dict(Nq=0), osattn.ERR_INVALID_ARG),
     (dict(scale=float("nan")), osattn.ERR_INVALID_ARG),
-    (dict(dtype=osattn.FP32), osattn.ERR_UNSUPPORTED),
+    (dict(dtype=3), osattn.ERR_UNSUPPORTED),
     (dict(d=96), osattn.ERR_UNSUPPORTED),
+    (dict(dtype=osattn.FP32, dv=P + 8), osattn.ERR_INVALID_ARG),
+    (dict(dtype=osattn.FP32, ws_bytes=8 * 4 - 1), osattn.ERR_INVALID_ARG),
 ])
 def test_bwd_host_validation(L, kw, expect):
     assert call_bwd(**kw) == expect
@@ -253,6 +255,8 @@ def test_bwd_strided_host_validation(L, slot, bad):
 def test_bwd_strided_shares_osattn_bwd_checks(L):
     assert call_bwd_strided(do=None) == osattn.ERR_INVALID_ARG
     assert call_bwd_strided(ws_bytes=2 * 8 * 4 - 1) == osattn.ERR_INVALID_ARG
-    assert call_bwd_strided(dtype=osattn.FP32) == osattn.ERR_UNSUPPORTED
+    assert call_bwd_strided(dtype=3) == osattn.ERR_UNSUPPORTED
+    # fp32 strides: multiples of 4 elements (16 bytes)
+    assert call_bwd_strided([(1024, 64, 66)] + [BNHD] * 7, dtype=osattn.FP32) == osattn.ERR_INVALID_ARG
     assert call_bwd_strided(d=96) == osattn.ERR_UNSUPPORTED
     assert call_bwd_strided((BNHD,) * 8, dv=P + 8) == osattn.ERR_INVALID_ARG

@@ -3,7 +3,12 @@ oracle's gradients, on the forward outputs (O, LSE) of the library itself.
 
 Gate per gradient tensor g (reading c18):
     |g - g_ref| <= 2e-2 |g_ref| + t * rms(g_ref) + half an ulp of g_ref + 1e-5,
-with t = 8e-2 for bf16 and 1.5e-2 for fp16.  The kernels round P and dS to
+with t = 8e-2 for bf16 and 1.5e-2 for fp16.  fp32 (SIMT kernels, fp32
+throughout) is gated by |g - g_ref| <= 1e-4 |g_ref| + 1e-4 rms(g_ref) + 1e-6:
+its only departures from exact arithmetic are fp32 roundings, and the
+largest of them, a d-term score dot product (relative error below
+d * 2^-24 of sum |q_k k_k|, about 8e-5 in the exponent for d = 128 and the
+inputs below), bounds the relative error of P and hence of each gradient.  The kernels round P and dS to
 the input type before the MMAs (unit roundoff u = 2^-9 for bf16, 2^-12 for
 fp16), read D from the 16-bit O of the forward pass, accumulate in fp32 and
 round the result once more.  Each row of dS sums to zero, so dQ and dK are
@@ -29,18 +34,21 @@ from _compare import half_ulp_bf16, half_ulp_fp16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-KIND = {torch.bfloat16: "bf16", torch.float16: "fp16"}
+KIND = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
 
 
-T_RMS = {"bf16": 8e-2, "fp16": 1.5e-2}
+T_RMS = {"bf16": 8e-2, "fp16": 1.5e-2, "fp32": 1e-4}
 
 
 def check_grad(g, ref, kind, name):
     g = np.asarray(g, dtype=np.float64)
     assert not np.isnan(g).any(), f"NaN in {name}"
     rms = math.sqrt(float((ref ** 2).mean())) if ref.size else 0.0
-    ulp = half_ulp_bf16(ref) if kind == "bf16" else half_ulp_fp16(ref)
-    gate = 2e-2 * np.abs(ref) + T_RMS[kind] * rms + ulp + 1e-5
+    if kind == "fp32":
+        gate = 1e-4 * np.abs(ref) + T_RMS[kind] * rms + 1e-6
+    else:
+        ulp = half_ulp_bf16(ref) if kind == "bf16" else half_ulp_fp16(ref)
+        gate = 2e-2 * np.abs(ref) + T_RMS[kind] * rms + ulp + 1e-5
     err = np.abs(g - ref)
     bad = err > gate
     assert not bad.any(), (f"{name}: error {err.max():.3e} over gate at {np.argwhere(bad)[:4].tolist()} "
@@ -175,5 +183,6 @@ def test_bwd_strided_matches_contiguous_bitwise(case, dtype):
                dq=outs[0], dk=outs[1], dv=outs[2])
     assert osattn.get_device_status() == osattn.OK
     torch.cuda.synchronize()
+    bits = torch.int32 if dtype == torch.float32 else torch.int16
     for a, b in zip((dq1, dk1, dv1), outs):
-        assert torch.equal(a.view(torch.int16), b.contiguous().view(torch.int16))
+        assert torch.equal(a.view(bits), b.contiguous().view(bits))
