@@ -23,11 +23,21 @@ __device__ unsigned int g_device_status[2];
 
 constexpr int kMaxDevices = 64;
 
+constexpr int kOffloadEvents = 64;  // event ring of the offload pipeline
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;  // device address of g_device_status
+  // Offload pipeline (osattn_fwd_offload), created on first use: a
+  // host-to-device and a device-to-host copy stream and their events.
+  bool offload_ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_entry = nullptr, ev_final = nullptr;
+  cudaEvent_t ev_in[kOffloadEvents] = {}, ev_out[kOffloadEvents] = {};
 };
+
+std::mutex g_offload_mutex;  // one offload enqueue at a time (shared streams and events)
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
@@ -252,9 +262,105 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
+int offload_streams(DeviceState* ds) {
+  if (ds->offload_ready) return OSATTN_OK;
+  const unsigned ef = cudaEventDisableTiming;
+  if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ds->ev_entry, ef) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ds->ev_final, ef) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  for (int i = 0; i < kOffloadEvents; ++i)
+    if (cudaEventCreateWithFlags(&ds->ev_in[i], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ds->ev_out[i], ef) != cudaSuccess)
+      return OSATTN_ERR_CUDA;
+  ds->offload_ready = true;
+  return OSATTN_OK;
+}
+
+// Host -> device -> host pipeline over chunks of heads: the copy of chunk
+// c + 1 in, the forward pass of chunk c and the copy of chunk c - 1 out run
+// concurrently on three streams.
+int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh,
+                     void* Qd, void* Kd, void* Vd, void* Od, float* LSEd, int B, int H, int Nq,
+                     int Nkv, int d, float scale, int causal, const int32_t* key_len, int dtype,
+                     int heads_per_chunk, void* stream) {
+  if (!Qh || !Kh || !Vh || !Oh || !LSEh) return OSATTN_ERR_INVALID_ARG;
+  int rc = validate_fwd(Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (heads_per_chunk < 0) return OSATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
+  if (rc != OSATTN_OK) return rc;
+  int hc = heads_per_chunk;
+  if (hc == 0) {
+    // Automatic: enough heads that a chunk's launch covers two waves of CTAs
+    // (256 query rows per CTA on the tensor cores, 16 in the fp32 kernel).
+    const int rows_per_cta = dtype == OSATTN_FP32 ? 16 : 256;
+    const long long units = (Nq + rows_per_cta - 1) / rows_per_cta;
+    hc = static_cast<int>((2LL * ds->num_sms + units - 1) / units);
+  }
+  if (hc > H) hc = H;
+  std::lock_guard<std::mutex> lock(g_offload_mutex);
+  rc = offload_streams(ds);
+  if (rc != OSATTN_OK) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t es = elem_size(dtype);
+  const size_t q_head = static_cast<size_t>(Nq) * d, kv_head = static_cast<size_t>(Nkv) * d;
+  // Copies wait for the caller's earlier work on `stream` (it may still be
+  // reading the device buffers).
+  if (cudaEventRecord(ds->ev_entry, cs) != cudaSuccess ||
+      cudaStreamWaitEvent(ds->h2d, ds->ev_entry, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(ds->d2h, ds->ev_entry, 0) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  int c = 0;
+  for (int b = 0; b < B; ++b) {
+    for (int h0 = 0; h0 < H; h0 += hc, ++c) {
+      const int nh = H - h0 < hc ? H - h0 : hc;
+      const size_t head0 = static_cast<size_t>(b) * H + h0;
+      const size_t qo = head0 * q_head * es, ko = head0 * kv_head * es;
+      const size_t qn = nh * q_head * es, kn = nh * kv_head * es;
+      cudaEvent_t ein = ds->ev_in[c % kOffloadEvents], eout = ds->ev_out[c % kOffloadEvents];
+      auto cp = [](void* dst, const void* src, size_t off, size_t n, cudaMemcpyKind kind,
+                   cudaStream_t s) {
+        return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
+                               n, kind, s);
+      };
+      if (cp(Qd, Qh, qo, qn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
+          cp(Kd, Kh, ko, kn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
+          cp(Vd, Vh, ko, kn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
+          cudaEventRecord(ein, ds->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, ein, 0) != cudaSuccess)
+        return OSATTN_ERR_CUDA;
+      rc = fwd_impl(static_cast<const char*>(Qd) + qo, static_cast<const char*>(Kd) + ko,
+                    static_cast<const char*>(Vd) + ko, static_cast<char*>(Od) + qo,
+                    LSEd + head0 * Nq, 1, nh, Nq, Nkv, d, nullptr, nullptr, nullptr, nullptr, scale,
+                    causal, key_len ? key_len + b : nullptr, dtype, cs);
+      if (rc != OSATTN_OK) return rc;
+      const size_t lo = head0 * Nq * sizeof(float), ln = nh * static_cast<size_t>(Nq) * sizeof(float);
+      if (cudaEventRecord(eout, cs) != cudaSuccess || cudaStreamWaitEvent(ds->d2h, eout, 0) != cudaSuccess ||
+          cp(Oh, Od, qo, qn, cudaMemcpyDeviceToHost, ds->d2h) != cudaSuccess ||
+          cp(LSEh, LSEd, lo, ln, cudaMemcpyDeviceToHost, ds->d2h) != cudaSuccess)
+        return OSATTN_ERR_CUDA;
+    }
+  }
+  // `stream` completes only after the last copy out.
+  if (cudaEventRecord(ds->ev_final, ds->d2h) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, ds->ev_final, 0) != cudaSuccess)
+    return OSATTN_ERR_CUDA;
+  return OSATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int osattn_fwd_offload(const void* Q_host, const void* K_host, const void* V_host, void* O_host,
+                       float* LSE_host, void* Q, void* K, void* V, void* O, float* LSE, int B,
+                       int H, int Nq, int Nkv, int d, float scale, int causal,
+                       const int32_t* key_len, int dtype, int heads_per_chunk, void* stream) {
+  return fwd_offload_impl(Q_host, K_host, V_host, O_host, LSE_host, Q, K, V, O, LSE, B, H, Nq, Nkv,
+                          d, scale, causal, key_len, dtype, heads_per_chunk, stream);
+}
 
 int osattn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,

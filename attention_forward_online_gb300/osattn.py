@@ -29,7 +29,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
            "osattn_splitkv_workspace_bytes", "osattn_fwd_splitkv_noalloc",
-           "osattn_bwd", "osattn_bwd_strided", "osattn_bwd_workspace_bytes", "osattn_softmax_rows",
+           "osattn_bwd", "osattn_bwd_strided", "osattn_bwd_workspace_bytes",
+           "osattn_fwd_offload", "osattn_softmax_rows",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -76,6 +77,9 @@ def lib():
             L.osattn_bwd_strided.argtypes = ([vp] * 9 + [i32] * 5 + [i64p] * 8 +
                                              [ctypes.c_float, i32, vp, i32, vp, ctypes.c_size_t, vp])
             L.osattn_bwd_strided.restype = i32
+            L.osattn_fwd_offload.argtypes = ([vp] * 10 + [i32] * 5 + [ctypes.c_float, i32, vp, i32,
+                                                                       i32, vp])
+            L.osattn_fwd_offload.restype = i32
             L.osattn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
             L.osattn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_softmax_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, vp]
@@ -220,6 +224,60 @@ def _check_qkv(q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
     return B, H, Nq, Nkv, d
+
+
+def fwd_offload(q_host, k_host, v_host, out_host=None, lse_host=None, q=None, k=None, v=None,
+                out=None, lse=None, scale: float | None = None, causal: bool = False,
+                key_len=None, heads_per_chunk: int = 0, stream=None):
+    """Attention forward of host tensors through osattn_fwd_offload: q_host
+    [B,H,Nq,d], k_host/v_host [B,H,Nkv,d] (contiguous CPU tensors, pinned for
+    the copies to overlap the compute) are copied in chunks of heads to the
+    device buffers q, k, v (allocated when not given), attended, and O/LSE are
+    copied back into out_host/lse_host (pinned CPU tensors, allocated when not
+    given).  Returns (out_host, lse_host); they are valid once `stream` has
+    synchronised.  key_len is a CUDA int32 tensor with B entries or None;
+    heads_per_chunk 0 lets the library size the chunks."""
+    import torch
+
+    for t in (q_host, k_host, v_host):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q_host, k_host, v_host must be contiguous 4-D CPU tensors")
+    B, H, Nq, d = q_host.shape
+    Nkv = k_host.shape[2]
+    if tuple(k_host.shape) != (B, H, Nkv, d) or tuple(v_host.shape) != (B, H, Nkv, d):
+        raise ValueError("k_host and v_host must be [B, H, Nkv, d] matching q_host")
+    if k_host.dtype != q_host.dtype or v_host.dtype != q_host.dtype:
+        raise TypeError("q_host, k_host, v_host must share one dtype")
+    dtype = _dtype_code(q_host)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) if q is None else q
+    k = torch.empty(k_host.shape, dtype=k_host.dtype, device=dev) if k is None else k
+    v = torch.empty(v_host.shape, dtype=v_host.dtype, device=dev) if v is None else v
+    out = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    if out_host is None:
+        out_host = torch.empty(q_host.shape, dtype=q_host.dtype).pin_memory()
+    if lse_host is None:
+        lse_host = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    for t, ref in ((q, q_host), (k, k_host), (v, v_host), (out, q_host), (out_host, q_host)):
+        if tuple(t.shape) != tuple(ref.shape) or t.dtype != ref.dtype or not t.is_contiguous():
+            raise ValueError("device buffers and out_host must be contiguous and match the inputs")
+    for t in (lse, lse_host):
+        if tuple(t.shape) != (B, H, Nq) or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("lse and lse_host must be contiguous fp32 [B, H, Nq]")
+    if out_host.is_cuda or lse_host.is_cuda or not all(t.is_cuda for t in (q, k, v, out, lse)):
+        raise ValueError("host tensors must be CPU tensors and staging buffers CUDA tensors")
+    key_len, kl_ptr = _key_len_ptr(key_len, B)
+    st = lib().osattn_fwd_offload(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                  out_host.data_ptr(), lse_host.data_ptr(), q.data_ptr(),
+                                  k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                                  Nq, Nkv, d, float(scale), int(bool(causal)), kl_ptr, dtype,
+                                  int(heads_per_chunk), _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_fwd_offload")
+    return out_host, lse_host
 
 
 def fwd_splitkv(q, k, v, num_splits: int, scale: float | None = None, causal: bool = False,

@@ -117,6 +117,40 @@ int osattn_fwd_strided(const void* Q, const void* K, const void* V, void* O, flo
                        const int64_t* o_strides, float scale, int causal,
                        const int32_t* key_len, int dtype, void* stream);
 
+/*
+ * osattn_fwd_offload - osattn_fwd for inputs and outputs that live in host
+ * memory: copies Q, K, V in, runs the forward pass and copies O and LSE out,
+ * pipelined over chunks of heads so that the copy of one chunk in, the
+ * attention of the previous one and the copy out of the one before that
+ * overlap (one host-to-device and one device-to-host stream of the
+ * library's, each chunk's attention on `stream`).  Same result as
+ * osattn_fwd on the copied data.
+ *
+ *   Q_host, K_host, V_host   host, contiguous [B, H, N, d] (read); pinned
+ *                            (page-locked) memory for the copies to overlap
+ *   O_host, LSE_host         host, contiguous [B, H, Nq, d] / [B, H, Nq] (written)
+ *   Q, K, V, O, LSE          device buffers of the same shapes (overwritten;
+ *                            used as staging, and hold the inputs and outputs
+ *                            afterwards); alignment as for osattn_fwd
+ *   B .. dtype               as for osattn_fwd (key_len is a device array)
+ *   heads_per_chunk          heads per pipeline chunk, within one batch entry
+ *                            (larger than H: one chunk per batch entry); 0
+ *                            picks enough heads for two waves of CTAs per
+ *                            chunk; negative -> OSATTN_ERR_INVALID_ARG
+ *   stream                   the copies wait for work enqueued on `stream`
+ *                            before the call, and `stream` completes only
+ *                            after the last copy out: synchronize `stream`
+ *                            (or wait on an event recorded on it) before
+ *                            reading O_host and LSE_host
+ *
+ * Errors as for osattn_fwd (a null host pointer is OSATTN_ERR_INVALID_ARG).
+ * Calls from several host threads are serialised while they enqueue.
+ */
+int osattn_fwd_offload(const void* Q_host, const void* K_host, const void* V_host, void* O_host,
+                       float* LSE_host, void* Q, void* K, void* V, void* O, float* LSE, int B,
+                       int H, int Nq, int Nkv, int d, float scale, int causal,
+                       const int32_t* key_len, int dtype, int heads_per_chunk, void* stream);
+
 /* Largest num_splits osattn_fwd_splitkv accepts. */
 #define OSATTN_MAX_SPLITS 128
 

@@ -260,3 +260,28 @@ def test_bwd_strided_shares_osattn_bwd_checks(L):
     assert call_bwd_strided([(1024, 64, 66)] + [BNHD] * 7, dtype=osattn.FP32) == osattn.ERR_INVALID_ARG
     assert call_bwd_strided(d=96) == osattn.ERR_UNSUPPORTED
     assert call_bwd_strided((BNHD,) * 8, dv=P + 8) == osattn.ERR_INVALID_ARG
+
+
+def call_offload(**kw):
+    a = dict(qh=P, kh=P, vh=P, oh=P, lh=P, q=P, k=P, v=P, o=P, lse=P, B=1, H=2, Nq=8, Nkv=8, d=64,
+             scale=0.125, causal=0, key_len=None, dtype=osattn.BF16, hpc=1)
+    a.update(kw)
+    return osattn.lib().osattn_fwd_offload(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["q"],
+                                           a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                           a["Nq"], a["Nkv"], a["d"], a["scale"], a["causal"],
+                                           a["key_len"], a["dtype"], a["hpc"],
+                                           ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qh=None), osattn.ERR_INVALID_ARG),
+    (dict(lh=None), osattn.ERR_INVALID_ARG),
+    (dict(o=None), osattn.ERR_INVALID_ARG),
+    (dict(q=P + 8), osattn.ERR_INVALID_ARG),
+    (dict(hpc=-1), osattn.ERR_INVALID_ARG),
+    (dict(Nkv=0), osattn.ERR_INVALID_ARG),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+    (dict(dtype=3), osattn.ERR_UNSUPPORTED),
+])
+def test_offload_host_validation(L, kw, expect):
+    assert call_offload(**kw) == expect
