@@ -278,35 +278,25 @@ int offload_streams(DeviceState* ds) {
   return OSATTN_OK;
 }
 
+// One tensor of an offload pipeline: host and device copies of a
+// contiguous [B, H, ...] tensor and the bytes of one head.
+struct OffloadSeg {
+  void* host;
+  void* dev;
+  size_t head_bytes;
+};
+
 // Host -> device -> host pipeline over chunks of heads: the copy of chunk
-// c + 1 in, the forward pass of chunk c and the copy of chunk c - 1 out run
-// concurrently on three streams.
-int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh,
-                     void* Qd, void* Kd, void* Vd, void* Od, float* LSEd, int B, int H, int Nq,
-                     int Nkv, int d, float scale, int causal, const int32_t* key_len, int dtype,
-                     int heads_per_chunk, void* stream) {
-  if (!Qh || !Kh || !Vh || !Oh || !LSEh) return OSATTN_ERR_INVALID_ARG;
-  int rc = validate_fwd(Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nkv, d, scale, key_len, dtype);
-  if (rc != OSATTN_OK) return rc;
-  if (heads_per_chunk < 0) return OSATTN_ERR_INVALID_ARG;
-  DeviceState* ds = nullptr;
-  rc = device_state(&ds);
-  if (rc != OSATTN_OK) return rc;
-  int hc = heads_per_chunk;
-  if (hc == 0) {
-    // Automatic: enough heads that a chunk's launch covers two waves of CTAs
-    // (256 query rows per CTA on the tensor cores, 16 in the fp32 kernel).
-    const int rows_per_cta = dtype == OSATTN_FP32 ? 16 : 256;
-    const long long units = (Nq + rows_per_cta - 1) / rows_per_cta;
-    hc = static_cast<int>((2LL * ds->num_sms + units - 1) / units);
-  }
-  if (hc > H) hc = H;
+// c + 1 in, the compute of chunk c and the copy of chunk c - 1 out run
+// concurrently on the library's two copy streams and the caller's stream.
+// compute(b, h0, nh) enqueues the work of heads h0 .. h0 + nh - 1 of batch
+// entry b on the caller's stream.
+template <typename Compute>
+int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
+                     int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
   std::lock_guard<std::mutex> lock(g_offload_mutex);
-  rc = offload_streams(ds);
+  int rc = offload_streams(ds);
   if (rc != OSATTN_OK) return rc;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const size_t es = elem_size(dtype);
-  const size_t q_head = static_cast<size_t>(Nq) * d, kv_head = static_cast<size_t>(Nkv) * d;
   // Copies wait for the caller's earlier work on `stream` (it may still be
   // reading the device buffers).
   if (cudaEventRecord(ds->ev_entry, cs) != cudaSuccess ||
@@ -318,29 +308,27 @@ int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, f
     for (int h0 = 0; h0 < H; h0 += hc, ++c) {
       const int nh = H - h0 < hc ? H - h0 : hc;
       const size_t head0 = static_cast<size_t>(b) * H + h0;
-      const size_t qo = head0 * q_head * es, ko = head0 * kv_head * es;
-      const size_t qn = nh * q_head * es, kn = nh * kv_head * es;
       cudaEvent_t ein = ds->ev_in[c % kOffloadEvents], eout = ds->ev_out[c % kOffloadEvents];
-      auto cp = [](void* dst, const void* src, size_t off, size_t n, cudaMemcpyKind kind,
-                   cudaStream_t s) {
-        return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
-                               n, kind, s);
-      };
-      if (cp(Qd, Qh, qo, qn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
-          cp(Kd, Kh, ko, kn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
-          cp(Vd, Vh, ko, kn, cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess ||
-          cudaEventRecord(ein, ds->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, ein, 0) != cudaSuccess)
+      for (int i = 0; i < n_in; ++i) {
+        const size_t off = head0 * ins[i].head_bytes;
+        if (cudaMemcpyAsync(static_cast<char*>(ins[i].dev) + off,
+                            static_cast<const char*>(ins[i].host) + off, nh * ins[i].head_bytes,
+                            cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess)
+          return OSATTN_ERR_CUDA;
+      }
+      if (cudaEventRecord(ein, ds->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, ein, 0) != cudaSuccess)
         return OSATTN_ERR_CUDA;
-      rc = fwd_impl(static_cast<const char*>(Qd) + qo, static_cast<const char*>(Kd) + ko,
-                    static_cast<const char*>(Vd) + ko, static_cast<char*>(Od) + qo,
-                    LSEd + head0 * Nq, 1, nh, Nq, Nkv, d, nullptr, nullptr, nullptr, nullptr, scale,
-                    causal, key_len ? key_len + b : nullptr, dtype, cs);
+      rc = compute(b, h0, nh);
       if (rc != OSATTN_OK) return rc;
-      const size_t lo = head0 * Nq * sizeof(float), ln = nh * static_cast<size_t>(Nq) * sizeof(float);
-      if (cudaEventRecord(eout, cs) != cudaSuccess || cudaStreamWaitEvent(ds->d2h, eout, 0) != cudaSuccess ||
-          cp(Oh, Od, qo, qn, cudaMemcpyDeviceToHost, ds->d2h) != cudaSuccess ||
-          cp(LSEh, LSEd, lo, ln, cudaMemcpyDeviceToHost, ds->d2h) != cudaSuccess)
+      if (cudaEventRecord(eout, cs) != cudaSuccess || cudaStreamWaitEvent(ds->d2h, eout, 0) != cudaSuccess)
         return OSATTN_ERR_CUDA;
+      for (int i = 0; i < n_out; ++i) {
+        const size_t off = head0 * outs[i].head_bytes;
+        if (cudaMemcpyAsync(static_cast<char*>(outs[i].host) + off,
+                            static_cast<const char*>(outs[i].dev) + off, nh * outs[i].head_bytes,
+                            cudaMemcpyDeviceToHost, ds->d2h) != cudaSuccess)
+          return OSATTN_ERR_CUDA;
+      }
     }
   }
   // `stream` completes only after the last copy out.
@@ -348,6 +336,95 @@ int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, f
       cudaStreamWaitEvent(cs, ds->ev_final, 0) != cudaSuccess)
     return OSATTN_ERR_CUDA;
   return OSATTN_OK;
+}
+
+// Heads per chunk: the caller's, or (0) enough that a chunk's launch covers
+// two waves of CTAs of `rows_per_cta` rows out of N.
+int offload_heads(int heads_per_chunk, int H, int N, int rows_per_cta, int num_sms) {
+  long long hc = heads_per_chunk;
+  if (hc == 0) {
+    const long long units = (N + rows_per_cta - 1) / rows_per_cta;
+    hc = (2LL * num_sms + units - 1) / units;
+  }
+  return static_cast<int>(hc < H ? hc : H);
+}
+
+int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh,
+                     void* Qd, void* Kd, void* Vd, void* Od, float* LSEd, int B, int H, int Nq,
+                     int Nkv, int d, float scale, int causal, const int32_t* key_len, int dtype,
+                     int heads_per_chunk, void* stream) {
+  if (!Qh || !Kh || !Vh || !Oh || !LSEh) return OSATTN_ERR_INVALID_ARG;
+  int rc = validate_fwd(Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (heads_per_chunk < 0) return OSATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
+  if (rc != OSATTN_OK) return rc;
+  // 256 query rows per CTA on the tensor cores, 16 in the fp32 kernel
+  const int hc = offload_heads(heads_per_chunk, H, Nq, dtype == OSATTN_FP32 ? 16 : 256, ds->num_sms);
+  const size_t es = elem_size(dtype);
+  const size_t qb = static_cast<size_t>(Nq) * d * es, kb = static_cast<size_t>(Nkv) * d * es;
+  const size_t lb = static_cast<size_t>(Nq) * sizeof(float);
+  const OffloadSeg ins[3] = {{const_cast<void*>(Qh), Qd, qb}, {const_cast<void*>(Kh), Kd, kb},
+                             {const_cast<void*>(Vh), Vd, kb}};
+  const OffloadSeg outs[2] = {{Oh, Od, qb}, {LSEh, LSEd, lb}};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return offload_pipeline(ds, cs, B, H, hc, ins, 3, outs, 2, [&](int b, int h0, int nh) {
+    const size_t head0 = static_cast<size_t>(b) * H + h0;
+    return fwd_impl(static_cast<const char*>(Qd) + head0 * qb, static_cast<const char*>(Kd) + head0 * kb,
+                    static_cast<const char*>(Vd) + head0 * kb, static_cast<char*>(Od) + head0 * qb,
+                    LSEd + head0 * Nq, 1, nh, Nq, Nkv, d, nullptr, nullptr, nullptr, nullptr, scale,
+                    causal, key_len ? key_len + b : nullptr, dtype, cs);
+  });
+}
+
+int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nkv, int d,
+             const int64_t* const* strides, float scale, int causal, const int32_t* key_len,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+int bwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, const void* Oh,
+                     const void* dOh, const float* LSEh, void* dQh, void* dKh, void* dVh, void* Qd,
+                     void* Kd, void* Vd, void* Od, void* dOd, float* LSEd, void* dQd, void* dKd,
+                     void* dVd, int B, int H, int Nq, int Nkv, int d, float scale, int causal,
+                     const int32_t* key_len, int dtype, void* workspace, size_t workspace_bytes,
+                     int heads_per_chunk, void* stream) {
+  if (!Qh || !Kh || !Vh || !Oh || !dOh || !LSEh || !dQh || !dKh || !dVh)
+    return OSATTN_ERR_INVALID_ARG;
+  // Argument checks of osattn_bwd on the whole tensors, before any copy.
+  int rc = validate_fwd(Qd, Kd, Vd, Od, LSEd, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (!dOd || !dQd || !dKd || !dVd || !aligned(dOd, 16) || !aligned(dQd, 16) || !aligned(dKd, 16) ||
+      !aligned(dVd, 16) || !workspace || !aligned(workspace, 16) ||
+      workspace_bytes < osattn_bwd_workspace_bytes(B, H, Nq) || heads_per_chunk < 0)
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  rc = device_state(&ds);
+  if (rc != OSATTN_OK) return rc;
+  // 128 keys per dK/dV CTA on the tensor cores, 32 in the fp32 kernels
+  const int hc = offload_heads(heads_per_chunk, H, Nkv, dtype == OSATTN_FP32 ? 32 : 128, ds->num_sms);
+  const size_t es = elem_size(dtype);
+  const size_t qb = static_cast<size_t>(Nq) * d * es, kb = static_cast<size_t>(Nkv) * d * es;
+  const size_t lb = static_cast<size_t>(Nq) * sizeof(float);
+  const OffloadSeg ins[6] = {{const_cast<void*>(Qh), Qd, qb},   {const_cast<void*>(Kh), Kd, kb},
+                             {const_cast<void*>(Vh), Vd, kb},   {const_cast<void*>(Oh), Od, qb},
+                             {const_cast<void*>(dOh), dOd, qb}, {const_cast<float*>(LSEh), LSEd, lb}};
+  const OffloadSeg outs[3] = {{dQh, dQd, qb}, {dKh, dKd, kb}, {dVh, dVd, kb}};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return offload_pipeline(ds, cs, B, H, hc, ins, 6, outs, 3, [&](int b, int h0, int nh) {
+    const size_t head0 = static_cast<size_t>(b) * H + h0;
+    auto at = [&](const void* base, size_t head_bytes) {
+      return static_cast<const char*>(base) + head0 * head_bytes;
+    };
+    auto at_w = [&](void* base, size_t head_bytes) {
+      return static_cast<char*>(base) + head0 * head_bytes;
+    };
+    // The chunk's D goes at the start of the workspace: chunks run in order
+    // on `stream`, so the next chunk overwrites it only after its readers.
+    return bwd_impl(at(Qd, qb), at(Kd, kb), at(Vd, kb), at(Od, qb), at(dOd, qb), LSEd + head0 * Nq,
+                    at_w(dQd, qb), at_w(dKd, kb), at_w(dVd, kb), 1, nh, Nq, Nkv, d, nullptr, scale,
+                    causal, key_len ? key_len + b : nullptr, dtype, workspace, workspace_bytes, cs);
+  });
 }
 
 }  // namespace
@@ -488,6 +565,18 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
                void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, d, nullptr, scale, causal,
                   key_len, dtype, workspace, workspace_bytes, stream);
+}
+
+int osattn_bwd_offload(const void* Q_host, const void* K_host, const void* V_host,
+                       const void* O_host, const void* dO_host, const float* LSE_host,
+                       void* dQ_host, void* dK_host, void* dV_host, void* Q, void* K, void* V,
+                       void* O, void* dO, float* LSE, void* dQ, void* dK, void* dV, int B, int H,
+                       int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
+                       int dtype, void* workspace, size_t workspace_bytes, int heads_per_chunk,
+                       void* stream) {
+  return bwd_offload_impl(Q_host, K_host, V_host, O_host, dO_host, LSE_host, dQ_host, dK_host,
+                          dV_host, Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nkv, d, scale, causal,
+                          key_len, dtype, workspace, workspace_bytes, heads_per_chunk, stream);
 }
 
 int osattn_bwd_strided(const void* Q, const void* K, const void* V, const void* O,

@@ -30,7 +30,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
            "osattn_splitkv_workspace_bytes", "osattn_fwd_splitkv_noalloc",
            "osattn_bwd", "osattn_bwd_strided", "osattn_bwd_workspace_bytes",
-           "osattn_fwd_offload", "osattn_softmax_rows",
+           "osattn_fwd_offload", "osattn_bwd_offload", "osattn_softmax_rows",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -80,6 +80,9 @@ def lib():
             L.osattn_fwd_offload.argtypes = ([vp] * 10 + [i32] * 5 + [ctypes.c_float, i32, vp, i32,
                                                                        i32, vp])
             L.osattn_fwd_offload.restype = i32
+            L.osattn_bwd_offload.argtypes = ([vp] * 18 + [i32] * 5 + [ctypes.c_float, i32, vp, i32,
+                                                                       vp, ctypes.c_size_t, i32, vp])
+            L.osattn_bwd_offload.restype = i32
             L.osattn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
             L.osattn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_softmax_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, vp]
@@ -359,6 +362,73 @@ def bwd(q, k, v, o, lse, do, scale: float | None = None, causal: bool = False, k
     if st != OK:
         raise OsattnError(st, what)
     return dq, dk, dv
+
+
+def bwd_offload(q_host, k_host, v_host, o_host, lse_host, do_host, scale: float | None = None,
+                causal: bool = False, key_len=None, dq_host=None, dk_host=None, dv_host=None,
+                device_buffers=None, workspace=None, heads_per_chunk: int = 0, stream=None):
+    """Gradients of host tensors through osattn_bwd_offload: inputs as for
+    bwd() but contiguous CPU tensors (pinned for the copies to overlap the
+    compute); dq_host, dk_host, dv_host are allocated (pinned) when not given.
+    device_buffers, if given, is a tuple of the nine contiguous CUDA staging
+    tensors (q, k, v, o, do, dq, dk, dv, lse); otherwise they are allocated.
+    Returns (dq_host, dk_host, dv_host), valid once `stream` has
+    synchronised."""
+    import torch
+
+    ins = (q_host, k_host, v_host, o_host, do_host)
+    for t in ins + (lse_host,):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous CPU tensors")
+    if q_host.dim() != 4:
+        raise ValueError("q_host must be [B, H, Nq, d]")
+    B, H, Nq, d = q_host.shape
+    Nkv = k_host.shape[2]
+    if tuple(k_host.shape) != (B, H, Nkv, d) or tuple(v_host.shape) != (B, H, Nkv, d):
+        raise ValueError("k_host and v_host must be [B, H, Nkv, d] matching q_host")
+    for t in (o_host, do_host):
+        if tuple(t.shape) != tuple(q_host.shape):
+            raise ValueError("o_host and do_host must be shaped like q_host")
+    for t in ins[1:]:
+        if t.dtype != q_host.dtype:
+            raise TypeError("host inputs must share one dtype")
+    if tuple(lse_host.shape) != (B, H, Nq) or lse_host.dtype != torch.float32:
+        raise ValueError("lse_host must be fp32 [B, H, Nq]")
+    dtype = _dtype_code(q_host)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if device_buffers is None:
+        mk = lambda ref: torch.empty(ref.shape, dtype=ref.dtype, device=dev)  # noqa: E731
+        device_buffers = (mk(q_host), mk(k_host), mk(v_host), mk(o_host), mk(do_host),
+                          mk(q_host), mk(k_host), mk(v_host), mk(lse_host))
+    qd, kd, vd, od, dod, dqd, dkd, dvd, lsed = device_buffers
+    for t, ref in zip(device_buffers, (q_host, k_host, v_host, o_host, do_host, q_host, k_host,
+                                       v_host, lse_host)):
+        if (not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(ref.shape)
+                or t.dtype != ref.dtype):
+            raise ValueError("device buffers must be contiguous CUDA tensors matching the inputs")
+    pin = lambda ref: torch.empty(ref.shape, dtype=ref.dtype).pin_memory()  # noqa: E731
+    dq_host = pin(q_host) if dq_host is None else dq_host
+    dk_host = pin(k_host) if dk_host is None else dk_host
+    dv_host = pin(v_host) if dv_host is None else dv_host
+    for t, ref in ((dq_host, q_host), (dk_host, k_host), (dv_host, v_host)):
+        if t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(ref.shape) or t.dtype != ref.dtype:
+            raise ValueError("dq_host, dk_host, dv_host must be contiguous CPU tensors matching the inputs")
+    need = bwd_workspace_bytes(B, H, Nq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    key_len, kl_ptr = _key_len_ptr(key_len, B)
+    st = lib().osattn_bwd_offload(
+        q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+        do_host.data_ptr(), lse_host.data_ptr(), dq_host.data_ptr(), dk_host.data_ptr(),
+        dv_host.data_ptr(), qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+        dod.data_ptr(), lsed.data_ptr(), dqd.data_ptr(), dkd.data_ptr(), dvd.data_ptr(), B, H, Nq,
+        Nkv, d, float(scale), int(bool(causal)), kl_ptr, dtype, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(heads_per_chunk), _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_bwd_offload")
+    return dq_host, dk_host, dv_host
 
 
 def softmax_rows(x, out=None, lse=None, want_lse: bool = True, stream=None):

@@ -488,7 +488,6 @@ def run_bwd(args, w):
 
     # end to end: inputs (q, k, v, O, LSE, dO) in, gradients out
     hin = [t.pin_memory() for t in (q, k, v, O.cpu(), L.cpu(), do)]
-    dins = [qd, kd, vd, O, L, dod]
     hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
     e2e_steps = max(3, min(args.steps, 20))
     es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
@@ -499,11 +498,10 @@ def run_bwd(args, w):
         for i in range(e2e_steps):
             flush.fill_(i & 0xFF)
             es[i].record(stream)
-            for dsrc, h in zip(dins, hin):
-                dsrc.copy_(h, non_blocking=True)
-            step()
-            for h, g in zip(hout, (dq, dk, dv)):
-                h.copy_(g, non_blocking=True)
+            osattn.bwd_offload(*hin, scale=w.scale, causal=w.causal, dq_host=hout[0],
+                               dk_host=hout[1], dv_host=hout[2],
+                               device_buffers=(qd, kd, vd, O, dod, dq, dk, dv, L), workspace=ws,
+                               stream=stream)
             ee[i].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -541,7 +539,7 @@ def run_bwd(args, w):
                                        f"rows and keys of {w.name}, fp64, {secs:.1f} s"},
             "e2e": {"value": round(world * w.bwd_flops / (e2e_ms * 1e-3) / 1e12, 3),
                     "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4), "api": "osattn_bwd_offload"},
             "gpu_launches": args.steps * 3,
             "clocks": clock_info,
         }

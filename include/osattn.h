@@ -271,6 +271,32 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * osattn_bwd_offload - osattn_bwd for tensors that live in host memory:
+ * copies Q, K, V, O, dO and LSE in, computes the gradients and copies dQ,
+ * dK and dV out, pipelined over chunks of heads exactly as
+ * osattn_fwd_offload.  Same results as osattn_bwd on the copied data.
+ *
+ *   *_host     host, contiguous (Q, O, dO, dQ [B, H, Nq, d]; K, V, dK, dV
+ *              [B, H, Nkv, d]; LSE [B, H, Nq] fp32); inputs read, dQ_host,
+ *              dK_host, dV_host written; pinned memory for the copies to
+ *              overlap the compute
+ *   Q .. dV    device buffers of the same shapes (overwritten staging)
+ *   B .. dtype, workspace, workspace_bytes   as for osattn_bwd
+ *   heads_per_chunk   as for osattn_fwd_offload (0: two waves of dK/dV
+ *              CTAs per chunk)
+ *   stream     as for osattn_fwd_offload
+ *
+ * Errors as for osattn_bwd (a null host pointer is OSATTN_ERR_INVALID_ARG).
+ */
+int osattn_bwd_offload(const void* Q_host, const void* K_host, const void* V_host,
+                       const void* O_host, const void* dO_host, const float* LSE_host,
+                       void* dQ_host, void* dK_host, void* dV_host, void* Q, void* K, void* V,
+                       void* O, void* dO, float* LSE, void* dQ, void* dK, void* dV, int B, int H,
+                       int Nq, int Nkv, int d, float scale, int causal, const int32_t* key_len,
+                       int dtype, void* workspace, size_t workspace_bytes, int heads_per_chunk,
+                       void* stream);
+
+/*
  * osattn_bwd_strided - osattn_bwd on tensors with arbitrary strides (e.g.
  * the [B, N, H, d] layout), without transposing copies.  Same computation,
  * results and errors as osattn_bwd.

@@ -285,3 +285,28 @@ def call_offload(**kw):
 ])
 def test_offload_host_validation(L, kw, expect):
     assert call_offload(**kw) == expect
+
+
+def call_bwd_offload(**kw):
+    a = dict(h=[P] * 9, d_=[P] * 9, B=1, H=2, Nq=8, Nkv=8, d=64, scale=0.125, causal=0,
+             key_len=None, dtype=osattn.BF16, ws=P, ws_bytes=1 << 20, hpc=0)
+    a.update(kw)
+    return osattn.lib().osattn_bwd_offload(*a["h"], *a["d_"], a["B"], a["H"], a["Nq"], a["Nkv"],
+                                           a["d"], a["scale"], a["causal"], a["key_len"],
+                                           a["dtype"], a["ws"], a["ws_bytes"], a["hpc"],
+                                           ctypes.c_void_p(None))
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(h=[P] * 8 + [None]), osattn.ERR_INVALID_ARG),          # dV_host
+    (dict(h=[None] + [P] * 8), osattn.ERR_INVALID_ARG),          # Q_host
+    (dict(d_=[P] * 4 + [None] + [P] * 4), osattn.ERR_INVALID_ARG),  # dO
+    (dict(d_=[P] * 8 + [P + 8]), osattn.ERR_INVALID_ARG),         # dV misaligned
+    (dict(ws=None), osattn.ERR_INVALID_ARG),
+    (dict(ws_bytes=2 * 8 * 4 - 1), osattn.ERR_INVALID_ARG),
+    (dict(hpc=-2), osattn.ERR_INVALID_ARG),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+    (dict(dtype=3), osattn.ERR_UNSUPPORTED),
+])
+def test_bwd_offload_host_validation(L, kw, expect):
+    assert call_bwd_offload(**kw) == expect

@@ -67,3 +67,28 @@ def test_offload_waits_for_earlier_work_on_the_stream():
     Od, Ld = osattn.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
     torch.cuda.synchronize()
     assert torch.equal(_bits(Oh), _bits(Od.cpu())) and torch.equal(Lh, Ld.cpu())
+
+
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
+@pytest.mark.parametrize("case", [
+    # B, H, Nq, Nkv, d, causal, key_len, heads_per_chunk
+    (2, 5, 300, 300, 128, True, None, 2),
+    (2, 3, 200, 333, 64, False, [333, 100], 0),
+], ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else "") + f"h{c[7]}")
+def test_bwd_offload_matches_device_call(case, dtype):
+    B, H, Nq, Nkv, d, causal, kl, hpc = case
+    q, k, v = make_qkv(B, H, Nq, Nkv, d, dtype, seed=6000 + H + Nq, q_std=1.5)
+    g = torch.Generator().manual_seed(6001)
+    do = torch.randn(B, H, Nq, d, generator=g).to(dtype)
+    kld = None if kl is None else torch.tensor(kl, dtype=torch.int32, device="cuda")
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = osattn.fwd(qd, kd, vd, scale=scale, causal=causal, key_len=kld)
+    ref = osattn.bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, key_len=kld)
+    torch.cuda.synchronize()
+    host = [t.pin_memory() for t in (q, k, v, o.cpu(), lse.cpu(), do)]
+    out = osattn.bwd_offload(*host, scale=scale, causal=causal, key_len=kld, heads_per_chunk=hpc)
+    torch.cuda.synchronize()
+    assert osattn.get_device_status() == osattn.OK
+    for a, b in zip(out, ref):
+        assert torch.equal(_bits(a), _bits(b.cpu()))
