@@ -427,9 +427,48 @@ int bwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, const void*
   });
 }
 
+int softmax_rows_offload_impl(const void* in_h, void* out_h, float* lse_h, void* in, void* out,
+                              float* lse, int64_t rows, int N, int dtype, int64_t rows_per_chunk,
+                              void* stream) {
+  if (!in_h || !out_h || !in || !out || rows < 1 || N < 1 || rows_per_chunk < 0 ||
+      (lse_h == nullptr) != (lse == nullptr) || rows > 0x7fffffffLL)
+    return OSATTN_ERR_INVALID_ARG;
+  if (dtype != OSATTN_BF16 && dtype != OSATTN_FP32 && dtype != OSATTN_FP16)
+    return OSATTN_ERR_UNSUPPORTED;
+  const uintptr_t el = elem_size(dtype);
+  if (!aligned(in, el) || !aligned(out, el) || (lse && !aligned(lse, 4)))
+    return OSATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != OSATTN_OK) return rc;
+  // Automatic: 16 chunks (the kernel is bound by memory, so the pipeline only
+  // has to keep both copy directions busy; more chunks shorten its fill).
+  int64_t rc_rows = rows_per_chunk ? rows_per_chunk : (rows + 15) / 16;
+  if (rc_rows > rows) rc_rows = rows;
+  const size_t rb = static_cast<size_t>(N) * el;
+  const OffloadSeg ins[1] = {{const_cast<void*>(in_h), in, rb}};
+  const OffloadSeg outs[2] = {{out_h, out, rb}, {lse_h, lse, sizeof(float)}};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return offload_pipeline(ds, cs, 1, static_cast<int>(rows), static_cast<int>(rc_rows), ins, 1, outs,
+                          lse ? 2 : 1, [&](int, int r0, int nr) {
+                            const size_t off = static_cast<size_t>(r0) * rb;
+                            const cudaError_t e = osattn::launch_softmax_rows(
+                                static_cast<const char*>(in) + off, static_cast<char*>(out) + off,
+                                lse ? lse + r0 : nullptr, nr, N, dtype, ds->num_sms, cs);
+                            return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+                          });
+}
+
 }  // namespace
 
 extern "C" {
+
+int osattn_softmax_rows_offload(const void* in_host, void* out_host, float* lse_host, void* in,
+                                void* out, float* lse, int64_t rows, int N, int dtype,
+                                int64_t rows_per_chunk, void* stream) {
+  return softmax_rows_offload_impl(in_host, out_host, lse_host, in, out, lse, rows, N, dtype,
+                                   rows_per_chunk, stream);
+}
 
 int osattn_fwd_offload(const void* Q_host, const void* K_host, const void* V_host, void* O_host,
                        float* LSE_host, void* Q, void* K, void* V, void* O, float* LSE, int B,

@@ -31,6 +31,7 @@ EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
            "osattn_splitkv_workspace_bytes", "osattn_fwd_splitkv_noalloc",
            "osattn_bwd", "osattn_bwd_strided", "osattn_bwd_workspace_bytes",
            "osattn_fwd_offload", "osattn_bwd_offload", "osattn_softmax_rows",
+           "osattn_softmax_rows_offload",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
            "osattn_last_timeout_site")
@@ -83,6 +84,9 @@ def lib():
             L.osattn_bwd_offload.argtypes = ([vp] * 18 + [i32] * 5 + [ctypes.c_float, i32, vp, i32,
                                                                        vp, ctypes.c_size_t, i32, vp])
             L.osattn_bwd_offload.restype = i32
+            L.osattn_softmax_rows_offload.argtypes = [vp] * 6 + [ctypes.c_int64, i32, i32,
+                                                                 ctypes.c_int64, vp]
+            L.osattn_softmax_rows_offload.restype = i32
             L.osattn_bwd_workspace_bytes.argtypes = [i32, i32, i32]
             L.osattn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.osattn_softmax_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, i32, vp]
@@ -452,6 +456,44 @@ def softmax_rows(x, out=None, lse=None, want_lse: bool = True, stream=None):
     if st != OK:
         raise OsattnError(st, "osattn_softmax_rows")
     return out, lse
+
+
+def softmax_rows_offload(x_host, out_host=None, lse_host=None, x=None, out=None, lse=None,
+                         want_lse: bool = True, rows_per_chunk: int = 0, stream=None):
+    """Row softmax of a contiguous CPU [rows, N] tensor (pinned for the copies
+    to overlap) through osattn_softmax_rows_offload; x/out/lse are the device
+    staging buffers (allocated when not given), out_host/lse_host the pinned
+    results (allocated when not given).  Returns (out_host, lse_host or None),
+    valid once `stream` has synchronised."""
+    import torch
+
+    if x_host.dim() != 2 or x_host.is_cuda or not x_host.is_contiguous():
+        raise ValueError("x_host must be a contiguous CPU [rows, N] tensor")
+    codes = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
+    if x_host.dtype not in codes:
+        raise TypeError("x_host must be bf16, fp16 or fp32")
+    rows, N = x_host.shape
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev) if x is None else x
+    out = torch.empty_like(x) if out is None else out
+    out_host = torch.empty(x_host.shape, dtype=x_host.dtype).pin_memory() if out_host is None else out_host
+    if want_lse:
+        lse = torch.empty(rows, dtype=torch.float32, device=dev) if lse is None else lse
+        lse_host = torch.empty(rows, dtype=torch.float32).pin_memory() if lse_host is None else lse_host
+    else:
+        lse = lse_host = None
+    for t in (x, out):
+        if not t.is_cuda or not t.is_contiguous() or t.shape != x_host.shape or t.dtype != x_host.dtype:
+            raise ValueError("x and out must be contiguous CUDA tensors shaped like x_host")
+    if out_host.is_cuda or not out_host.is_contiguous() or out_host.shape != x_host.shape:
+        raise ValueError("out_host must be a contiguous CPU tensor shaped like x_host")
+    st = lib().osattn_softmax_rows_offload(
+        x_host.data_ptr(), out_host.data_ptr(), None if lse_host is None else lse_host.data_ptr(),
+        x.data_ptr(), out.data_ptr(), None if lse is None else lse.data_ptr(), rows, N,
+        codes[x_host.dtype], int(rows_per_chunk), _stream_handle(stream))
+    if st != OK:
+        raise OsattnError(st, "osattn_softmax_rows_offload")
+    return out_host, lse_host
 
 
 def get_device_status(stream=None) -> int:

@@ -344,6 +344,29 @@ int osattn_bwd_strided(const void* Q, const void* K, const void* V, const void* 
 int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int N, int dtype,
                         void* stream);
 
+/*
+ * osattn_softmax_rows_offload - osattn_softmax_rows for a matrix in host
+ * memory: copies it in, normalises and copies y (and LSE) out, pipelined
+ * over chunks of rows as osattn_fwd_offload does over heads.  Same result as
+ * osattn_softmax_rows on the copied data.
+ *
+ *   in_host    host, [rows, N] row-major, element type `dtype` (read); pinned
+ *              memory for the copies to overlap
+ *   out_host   host, [rows, N] (written)
+ *   lse_host   host fp32 [rows] (written) or NULL; NULL exactly when `lse` is
+ *   in, out, lse   device buffers of the same shapes (overwritten staging)
+ *   rows_per_chunk   rows per pipeline chunk; 0 picks 16 chunks; negative ->
+ *              OSATTN_ERR_INVALID_ARG
+ *   stream     as for osattn_fwd_offload
+ *
+ * Errors as for osattn_softmax_rows (null host pointers, or lse_host and lse
+ * not both given or both NULL: OSATTN_ERR_INVALID_ARG; rows above 2^31 - 1:
+ * OSATTN_ERR_INVALID_ARG).
+ */
+int osattn_softmax_rows_offload(const void* in_host, void* out_host, float* lse_host, void* in,
+                                void* out, float* lse, int64_t rows, int N, int dtype,
+                                int64_t rows_per_chunk, void* stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char* osattn_status_string(int status);
 

@@ -310,3 +310,16 @@ def call_bwd_offload(**kw):
 ])
 def test_bwd_offload_host_validation(L, kw, expect):
     assert call_bwd_offload(**kw) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, P, P, P, P, P, 4, 8, osattn.BF16, 0), osattn.ERR_INVALID_ARG),   # in_host
+    ((P, P, None, P, P, P, 4, 8, osattn.BF16, 0), osattn.ERR_INVALID_ARG),   # lse_host without lse
+    ((P, P, P, P, P, None, 4, 8, osattn.BF16, 0), osattn.ERR_INVALID_ARG),   # lse without lse_host
+    ((P, P, P, P, P, P, 0, 8, osattn.BF16, 0), osattn.ERR_INVALID_ARG),      # rows
+    ((P, P, P, P, P, P, 4, 8, osattn.BF16, -1), osattn.ERR_INVALID_ARG),     # rows_per_chunk
+    ((P, P, P, P + 1, P, P, 4, 8, osattn.BF16, 0), osattn.ERR_INVALID_ARG),  # misaligned in
+    ((P, P, P, P, P, P, 4, 8, 7, 0), osattn.ERR_UNSUPPORTED),
+])
+def test_softmax_rows_offload_host_validation(L, args, expect):
+    assert L.osattn_softmax_rows_offload(*args, ctypes.c_void_p(None)) == expect

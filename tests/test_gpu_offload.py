@@ -92,3 +92,18 @@ def test_bwd_offload_matches_device_call(case, dtype):
     assert osattn.get_device_status() == osattn.OK
     for a, b in zip(out, ref):
         assert torch.equal(_bits(a), _bits(b.cpu()))
+
+
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
+@pytest.mark.parametrize("shape,rpc", [((1000, 4096), 0), ((37, 50000), 5), ((300, 1000), 64)])
+def test_softmax_rows_offload_matches_device_call(shape, rpc, dtype):
+    g = torch.Generator().manual_seed(71)
+    x = (torch.randn(*shape, generator=g) * 3).to(dtype)
+    yh, lh = osattn.softmax_rows_offload(x.pin_memory(), rows_per_chunk=rpc)
+    torch.cuda.synchronize()
+    yd, ld = osattn.softmax_rows(x.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(yh), _bits(yd.cpu())) and torch.equal(lh, ld.cpu())
+    yh2, none = osattn.softmax_rows_offload(x.pin_memory(), want_lse=False, rows_per_chunk=rpc)
+    torch.cuda.synchronize()
+    assert none is None and torch.equal(_bits(yh2), _bits(yd.cpu()))
