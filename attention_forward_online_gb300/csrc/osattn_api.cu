@@ -292,11 +292,9 @@ struct OffloadSeg {
 // compute(b, h0, nh) enqueues the work of heads h0 .. h0 + nh - 1 of batch
 // entry b on the caller's stream.
 template <typename Compute>
-int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
-                     int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
-  std::lock_guard<std::mutex> lock(g_offload_mutex);
-  int rc = offload_streams(ds);
-  if (rc != OSATTN_OK) return rc;
+int offload_enqueue(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
+                    int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
+  int rc = OSATTN_OK;
   // Copies wait for the caller's earlier work on `stream` (it may still be
   // reading the device buffers).
   if (cudaEventRecord(ds->ev_entry, cs) != cudaSuccess ||
@@ -331,11 +329,27 @@ int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, con
       }
     }
   }
-  // `stream` completes only after the last copy out.
-  if (cudaEventRecord(ds->ev_final, ds->d2h) != cudaSuccess ||
-      cudaStreamWaitEvent(cs, ds->ev_final, 0) != cudaSuccess)
-    return OSATTN_ERR_CUDA;
   return OSATTN_OK;
+}
+
+// offload_enqueue under the offload mutex (the copy streams and events are
+// shared), with both copy streams joined back into `stream` on every exit.
+template <typename Compute>
+int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
+                     int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
+  std::lock_guard<std::mutex> lock(g_offload_mutex);
+  int rc = offload_streams(ds);
+  if (rc != OSATTN_OK) return rc;
+  rc = offload_enqueue(ds, cs, B, H, hc, ins, n_in, outs, n_out, compute);
+  // `stream` completes only after the last copy, in either direction, even
+  // when the enqueue stopped part way (the caller may free the buffers once
+  // `stream` is done).
+  bool joined = true;
+  for (cudaStream_t cp : {ds->h2d, ds->d2h})
+    joined = joined && cudaEventRecord(ds->ev_final, cp) == cudaSuccess &&
+             cudaStreamWaitEvent(cs, ds->ev_final, 0) == cudaSuccess;
+  if (rc != OSATTN_OK) return rc;
+  return joined ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
 // Heads per chunk: the caller's, or (0) enough that a chunk's launch covers
