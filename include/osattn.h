@@ -1,7 +1,7 @@
 /*
  * osattn.h - C ABI of libosattn, a fused scaled-dot-product attention forward
  * pass for one NVIDIA GB300 (sm_103a), built on the one-pass online-softmax
- * normaliser.
+ * normaliser, with its backward pass and the standalone row softmax.
  *
  * Sources (cited by page title and section):
  *   [Ch6]  "CUDA 算子工程：手写 FlashAttention v2 之路", chapter 6
@@ -13,6 +13,15 @@
  *          FlashAttention): the attention problem statement (§1.1), the
  *          inner loop with scale and mask and the single final O / l (§4.1),
  *          the causal diagonal-block pitfall (§6.3).
+ *
+ * Entry points:
+ *   forward        osattn_fwd, osattn_fwd_strided (any (b, h, row) strides),
+ *                  osattn_fwd_splitkv / _noalloc (key axis split and merged),
+ *                  osattn_fwd_offload (host-memory tensors, pipelined copies)
+ *   backward       osattn_bwd, osattn_bwd_strided, osattn_bwd_offload
+ *   row softmax    osattn_softmax_rows, osattn_softmax_rows_offload
+ *   helpers        workspace sizes, status strings, the device status word,
+ *                  the version, and test hooks for the bounded waits
  *
  * Every entry point is callable from C; no C++ or framework types cross it.
  */
