@@ -7,8 +7,9 @@ Inputs are the seeded synthetic tensors of the named workload, resident on
 cuda:0 before the first launch; --heads keeps only the first H heads (a
 smaller case of the same kernel for detailed Nsight Compute captures).  A
 backward workload runs the forward pass once, untimed, and then times the
-backward call (its three kernels).  Prints the median launch time from
-CUDA events on the launching stream.
+backward call (its three kernels).  A row-softmax workload runs
+osattn_softmax_rows (--heads then keeps that many thousand rows).  Prints
+the median launch time from CUDA events on the launching stream.
 """
 import argparse
 import dataclasses
@@ -24,10 +25,11 @@ def main(argv=None):
     import torch
 
     from attention_forward_online_gb300 import osattn
-    from attention_forward_online_gb300.inputs import (BWD_WORKLOADS, SPLITKV_WORKLOADS, WORKLOADS,
-                                                       make_grad_out, make_inputs)
+    from attention_forward_online_gb300.inputs import (BWD_WORKLOADS, ROW_WORKLOADS,
+                                                       SPLITKV_WORKLOADS, WORKLOADS,
+                                                       make_grad_out, make_inputs, make_rows)
 
-    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS, **BWD_WORKLOADS)
+    allw = dict(WORKLOADS, **SPLITKV_WORKLOADS, **BWD_WORKLOADS, **ROW_WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", required=True, choices=sorted(allw))
     ap.add_argument("--launches", type=int, default=4)
@@ -36,6 +38,8 @@ def main(argv=None):
                     help="key ranges for the split-KV entry point (0: unsplit; default: the workload's)")
     args = ap.parse_args(argv)
     w = allw[args.workload]
+    if args.workload in ROW_WORKLOADS:
+        return run_rows(w, args)
     if args.splits >= 0:
         w = dataclasses.replace(w, splits=args.splits)
     if args.heads:
@@ -81,6 +85,34 @@ def main(argv=None):
     print(f"{w.name} H={w.H} splits={w.splits}: launches {args.launches}, median {med:.4f} ms = "
           f"{flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
           f"ms {['%.4f' % m for m in ms]}")
+    return 0
+
+
+def run_rows(w, args):
+    import dataclasses
+
+    import torch
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import make_rows
+
+    if args.heads:
+        w = dataclasses.replace(w, rows=min(w.rows, 1000 * args.heads))
+    xd = make_rows(w).to("cuda:0")
+    yd = torch.empty_like(xd)
+    ld = torch.empty(w.rows, dtype=torch.float32, device=xd.device)
+    s = torch.cuda.Stream(device=xd.device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.launches)]
+    with torch.cuda.stream(s):
+        for i in range(args.launches):
+            ev[2 * i].record(s)
+            osattn.softmax_rows(xd, out=yd, lse=ld, stream=s)
+            ev[2 * i + 1].record(s)
+    s.synchronize()
+    ms = sorted(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(1, args.launches))
+    med = ms[len(ms) // 2] if ms else 0.0
+    print(f"{w.name} rows={w.rows}: launches {args.launches}, median {med:.4f} ms = "
+          f"{w.bytes_moved / (med * 1e-3) / 1e9:.0f} GB/s (first launch excluded)")
     return 0
 
 
