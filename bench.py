@@ -53,6 +53,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ("fwd_bf16_tcgen05.cu", "sm100_ptx.cuh", "tc_attn_mma.cuh")
 
 
+def fwd_config(w, world):
+    """The forward line's `config`, shared by both arms."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "d": w.d,
+            "causal": w.causal, "key_len": w.key_len, "splits": w.splits, "flops_per_step": w.flops,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -236,8 +244,7 @@ def run_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv, "d": w.d,
-                   "causal": w.causal, "parallelism": "replicas"},
+        "config": fwd_config(w, world),
         "cpu_baseline": {"value": round(tflops, 6), "unit": "TFLOPS", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(tflops, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -366,13 +373,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if w.dtype == "bf16" else "fp32", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nkv": w.Nkv,
-                       "d": w.d, "causal": w.causal, "key_len": w.key_len,
-                       "splits": w.splits,
-                       "flops_per_step": w.flops,
-                       "l2": "flushed between timed steps (256 MiB write)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "dtype": w.dtype, "data": "synthetic",
+            "config": fwd_config(w, world),
             "pct_of_bf16_peak": round(100 * value / world / peak, 2),
             "pct_of_bf16_peak_sustained": round(
                 100 * value / world / float(peaks["bf16_tflops_sustained"]), 2),
