@@ -228,7 +228,10 @@ def run_reference(args, w):
     from attention_forward_online_gb300.inputs import make_inputs
 
     q, k, v, _ = make_inputs(w)
-    n_rows = calibrate_rows(w, q, k, v, target_s=4.0, seed=1)
+    # Each step is a bounded row sample: about two minutes for the whole run
+    # (K + W steps), at most 4 s a step.
+    per_step = max(0.05, min(4.0, 120.0 / max(1, args.steps + args.warmup)))
+    n_rows = calibrate_rows(w, q, k, v, target_s=per_step, seed=1)
     for s in range(args.warmup):
         oracle_sample(w, q, k, v, n_rows, seed=100 + s)
     flops, secs = 0, 0.0
