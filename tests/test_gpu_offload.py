@@ -107,3 +107,42 @@ def test_softmax_rows_offload_matches_device_call(shape, rpc, dtype):
     yh2, none = osattn.softmax_rows_offload(x.pin_memory(), want_lse=False, rows_per_chunk=rpc)
     torch.cuda.synchronize()
     assert none is None and torch.equal(_bits(yh2), _bits(yd.cpu()))
+
+
+def test_offload_fully_masked_batch_and_oversized_chunks():
+    # A batch entry with key_len 0 (O = 0, LSE = -inf, no NaN) and
+    # heads_per_chunk above H (one chunk per batch entry).
+    B, H, N, d = 2, 3, 200, 64
+    q, k, v = make_qkv(B, H, N, N, d, torch.bfloat16, seed=81)
+    kld = torch.tensor([N, 0], dtype=torch.int32, device="cuda")
+    Oh, Lh = osattn.fwd_offload(q.pin_memory(), k.pin_memory(), v.pin_memory(), key_len=kld,
+                                heads_per_chunk=100)
+    torch.cuda.synchronize()
+    assert torch.all(Oh[1] == 0) and torch.all(torch.isneginf(Lh[1]))
+    assert torch.isfinite(Oh.float()).all() and torch.isfinite(Lh[0]).all()
+    Od, Ld = osattn.fwd(q.cuda(), k.cuda(), v.cuda(), key_len=kld)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(Oh), _bits(Od.cpu())) and torch.equal(Lh, Ld.cpu())
+
+
+def test_offload_reuses_buffers_across_calls():
+    # Two calls in a row on the same staging buffers and stream: the second
+    # call's copies in must wait for the first call's copies out.
+    B, H, N, d = 1, 6, 512, 128
+    s = torch.cuda.Stream()
+    bufs = None
+    outs = []
+    for seed in (91, 92):
+        q, k, v = make_qkv(B, H, N, N, d, torch.bfloat16, seed=seed)
+        if bufs is None:
+            bufs = [torch.empty_like(t, device="cuda") for t in (q, k, v, q)] + [
+                torch.empty((B, H, N), dtype=torch.float32, device="cuda")]
+        Oh, Lh = osattn.fwd_offload(q.pin_memory(), k.pin_memory(), v.pin_memory(), q=bufs[0],
+                                    k=bufs[1], v=bufs[2], out=bufs[3], lse=bufs[4], causal=True,
+                                    heads_per_chunk=2, stream=s)
+        outs.append((q, k, v, Oh, Lh))
+    s.synchronize()
+    for q, k, v, Oh, Lh in outs:
+        Od, Ld = osattn.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(Oh), _bits(Od.cpu())) and torch.equal(Lh, Ld.cpu())
