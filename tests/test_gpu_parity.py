@@ -202,3 +202,23 @@ def test_wait_timeout_reports_status_and_recovers():
     O, Lg = run_gpu(q, k, v, 0.125, True, None)
     Oref, Lref = oracle.attention_fwd(q, k, v, 0.125, True)
     check(O, Lg, Oref, Lref, "bf16")
+
+
+@pytest.mark.parametrize("name", ["bf16_causal_b4_h16_n4096_d64", "bf16_b8_h40_n2048_d128",
+                                  "bf16_causal_b1_h32_n16384_d128_qstd3"])
+def test_config_full_size_every_row(name):
+    # The three large workloads at full size, every output row against the
+    # oracle (about 3 TFLOP of fp64 work in all, multithreaded over rows),
+    # in the launch configuration the bench times.
+    w = WORKLOADS[name]
+    q, k, v, kl = make_inputs(w)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    O = torch.full_like(qd, float("nan"))
+    L = torch.full((w.B, w.H, w.Nq), float("nan"), dtype=torch.float32, device=DEV)
+    osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, out=O, lse=L)
+    assert osattn.get_device_status() == osattn.OK
+    Og = O.double().cpu().numpy()
+    Lg = L.double().cpu().numpy()
+    del O, L
+    Oref, Lref = oracle.attention_fwd(q, k, v, w.scale, w.causal, None)
+    print(name, "every row", check(Og, Lg, Oref, Lref, "bf16"))
