@@ -119,6 +119,7 @@ struct Params {
   int H, Nq, Nkv, BH;
   int num_splits;
   int num_q_blocks;  // ceil(Nq / 256)
+  int group_heads;   // causal, unsplit: heads per longest-first group of units
   float scale_log2;  // scale * log2(e)
   int causal;
   unsigned int* status;
@@ -529,15 +530,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Work unit: 256 query rows (two tiles) of one (b, h).  Units of a head
   // are adjacent in launch order so concurrently running CTAs share that
-  // head's K/V in L2; causal heads start with their longest units.
+  // head's K/V in L2.  Causal units differ in length; unsplit, they run
+  // longest first within groups of group_heads heads (whose K/V fits in L2
+  // together), so the launch does not end on the last heads' longest units.
   int unit = blockIdx.x, split = 0;
   if constexpr (kSplit) {  // key-range split fastest: splits of one unit run together
     split = unit % p.num_splits;
     unit /= p.num_splits;
   }
-  const int bh = unit / p.num_q_blocks;
-  int qb = unit % p.num_q_blocks;
-  if (p.causal) qb = p.num_q_blocks - 1 - qb;
+  int bh, qb;
+  if (!kSplit && p.causal) {
+    const int nqb = p.num_q_blocks, G = p.group_heads;
+    const int g0 = (unit / (G * nqb)) * G;    // first head of this unit's group
+    const int gsize = min(G, p.BH - g0);      // the last group may be smaller
+    const int r = unit - g0 * nqb;            // rank within the group
+    bh = g0 + r % gsize;
+    qb = nqb - 1 - r / gsize;                 // rank 0: the longest units
+  } else {
+    bh = unit / p.num_q_blocks;
+    qb = unit % p.num_q_blocks;
+    if (p.causal) qb = p.num_q_blocks - 1 - qb;
+  }
   const int b = bh / p.H, h = bh % p.H;
   int kv_len = p.Nkv;
   if (p.key_len) kv_len = min(max(p.key_len[b], 0), p.Nkv);
@@ -667,6 +680,13 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
   p.BH = a.B * a.H;
   p.num_splits = a.num_splits > 0 ? a.num_splits : 1;
   p.num_q_blocks = (a.Nq + kQTiles * BM - 1) / (kQTiles * BM);
+  {
+    // heads whose K and V together take about kGroupKVBytes of L2
+    constexpr long long kGroupKVBytes = 64ll << 20;
+    const long long kv_head = 2ll * a.Nkv * a.d * 2;
+    const long long gh = kGroupKVBytes / (kv_head > 0 ? kv_head : 1);
+    p.group_heads = static_cast<int>(gh < 1 ? 1 : (gh > p.BH ? p.BH : gh));
+  }
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.causal = a.causal;
   p.status = a.status;
