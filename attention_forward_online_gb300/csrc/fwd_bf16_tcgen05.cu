@@ -682,7 +682,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
   p.num_q_blocks = (a.Nq + kQTiles * BM - 1) / (kQTiles * BM);
   {
     // heads whose K and V together take about kGroupKVBytes of L2
-    constexpr long long kGroupKVBytes = 64ll << 20;
+    constexpr long long kGroupKVBytes = 32ll << 20;
     const long long kv_head = 2ll * a.Nkv * a.d * 2;
     const long long gh = kGroupKVBytes / (kv_head > 0 ? kv_head : 1);
     p.group_heads = static_cast<int>(gh < 1 ? 1 : (gh > p.BH ? p.BH : gh));
