@@ -115,6 +115,8 @@ struct BwdParams {
   const int32_t* key_len;
   int H, Nq, Nkv;
   int num_tiles;     // 128-row tiles per (b, h): of keys (dK/dV) or queries (dQ)
+  int BH;            // B * H
+  int group_heads;   // causal: heads per longest-first group of CTAs
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
@@ -142,6 +144,26 @@ __device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t tx_byte
   asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(tx_bytes)
                : "memory");
+}
+
+// The (b, h) and the rank by length (0 = longest loop) of this CTA's tile.
+// Causal tiles differ in length: they run longest first within groups of
+// group_heads heads (whose streamed tiles fit in L2 together), so the
+// launch does not end on the last heads' longest loops.  Otherwise heads
+// run one after another.
+__device__ __forceinline__ void unit_of(const BwdParams& p, int& bh, int& rank) {
+  const int nt = p.num_tiles;
+  if (p.causal) {
+    const int G = p.group_heads;
+    const int g0 = (static_cast<int>(blockIdx.x) / (G * nt)) * G;
+    const int gsize = min(G, p.BH - g0);
+    const int r = static_cast<int>(blockIdx.x) - g0 * nt;
+    bh = g0 + r % gsize;
+    rank = r / gsize;
+  } else {
+    bh = static_cast<int>(blockIdx.x) / nt;
+    rank = static_cast<int>(blockIdx.x) % nt;
+  }
 }
 
 __device__ __forceinline__ int clamp_key_len(const int32_t* key_len, int b, int Nkv) {
@@ -329,8 +351,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kDkdvRegion);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x / p.num_tiles;
-  const int kt = blockIdx.x % p.num_tiles;  // key tile 0 first: it meets the most query tiles
+  int bh, kt;
+  unit_of(p, bh, kt);  // causal: key tile 0 meets the most query tiles
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = kt * kT;
   const int kv_len = clamp_key_len(p.key_len, b, p.Nkv);
@@ -595,9 +617,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kDqRegion);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x / p.num_tiles;
-  int qt = blockIdx.x % p.num_tiles;
-  if (p.causal) qt = p.num_tiles - 1 - qt;  // the longest key loops first
+  int bh, qt;
+  unit_of(p, bh, qt);
+  if (p.causal) qt = p.num_tiles - 1 - qt;  // the last query tile has the longest key loop
   const int b = bh / p.H, h = bh % p.H;
   const int q0 = qt * kT;
   const int kv_len = clamp_key_len(p.key_len, b, p.Nkv);
@@ -811,10 +833,22 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
   using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
   cudaError_t e = launch_rowdot<T>(a);
   if (e != cudaSuccess) return e;
+  // Causal CTA groups: heads whose streamed tiles (Q and dO for dK/dV, K
+  // and V for dQ) take about 32 MB of L2 together.
+  auto group = [&](int rows) {
+    const long long head = 2ll * rows * a.d * 2;
+    const long long g = (32ll << 20) / (head > 0 ? head : 1);
+    const long long bh = static_cast<long long>(a.B) * a.H;
+    return static_cast<int>(g < 1 ? 1 : (g > bh ? bh : g));
+  };
   BwdParams pk = base;
+  pk.BH = a.B * a.H;
+  pk.group_heads = group(a.Nq);
   pk.num_tiles = (a.Nkv + kT - 1) / kT;
   const long long gk = static_cast<long long>(pk.num_tiles) * a.B * a.H;
   BwdParams pq = base;
+  pq.BH = a.B * a.H;
+  pq.group_heads = group(a.Nkv);
   pq.num_tiles = (a.Nq + kT - 1) / kT;
   const long long gq = static_cast<long long>(pq.num_tiles) * a.B * a.H;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -857,6 +891,8 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorM
   p.Nq = a.Nq;
   p.Nkv = a.Nkv;
   p.num_tiles = 0;
+  p.BH = a.B * a.H;
+  p.group_heads = 1;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
