@@ -222,3 +222,33 @@ def test_config_full_size_every_row(name):
     del O, L
     Oref, Lref = oracle.attention_fwd(q, k, v, w.scale, w.causal, None)
     print(name, "every row", check(Og, Lg, Oref, Lref, "bf16"))
+
+
+def test_causal_unit_groups_with_a_partial_last_group():
+    # Causal units run longest first within groups of heads sized to 32 MB
+    # of K/V: at N = 8192, d = 128 a group is 8 heads, so 12 heads make a
+    # full group and a partial one.  Every unit must be computed (outputs
+    # are NaN-prefilled) and sampled rows must match the oracle.
+    B, H, N, d = 1, 12, 8192, 128
+    q, k, v = make_qkv(B, H, N, N, d, torch.bfloat16, seed=123, q_std=2.0)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    O = torch.full_like(qd, float("nan"))
+    L = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=DEV)
+    scale = 1 / math.sqrt(d)
+    osattn.fwd(qd, kd, vd, scale=scale, causal=True, out=O, lse=L)
+    assert osattn.get_device_status() == osattn.OK
+    assert not torch.isnan(O).any().item() and torch.isfinite(L).all().item()
+    rows = sample_rows(B, H, N, 600, seed=5)
+    Oref, Lref = oracle.attention_fwd(q, k, v, scale, True, None, rows=rows)
+    idx = torch.tensor(rows, device=DEV)
+    check(O.reshape(-1, d)[idx].double().cpu().numpy(), L.reshape(-1)[idx].double().cpu().numpy(),
+          Oref, Lref, "bf16")
+    # the backward kernels order their causal CTAs the same way
+    g = torch.Generator().manual_seed(124)
+    dod = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).to(DEV)
+    grads = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]
+    osattn.bwd(qd, kd, vd, O, L, dod, scale=scale, causal=True, dq=grads[0], dk=grads[1],
+               dv=grads[2])
+    assert osattn.get_device_status() == osattn.OK
+    for t in grads:
+        assert torch.isfinite(t.float()).all().item()
