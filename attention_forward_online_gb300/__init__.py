@@ -1,4 +1,5 @@
-"""libosattn for GB300: fused attention forward with online softmax.
+"""libosattn for GB300: fused attention forward with online softmax, its
+backward pass and the standalone row softmax.
 
 The compute lives in hand-written CUDA kernels (csrc/) behind the C ABI in
 include/osattn.h; ``osattn`` is the ctypes binding.  Importing this package

@@ -1,10 +1,12 @@
 """ctypes binding for libosattn (argument marshalling only).
 
-Every step of the forward pass runs in the library's CUDA kernels; this
-module checks tensor shapes, allocates outputs with torch (device memory is
-torch's job here), and passes raw pointers and the current stream through
-the C ABI declared in include/osattn.h.  If libosattn.so is missing the calls
-raise: there is no fallback implementation.
+Every step of the forward pass, the backward pass and the row softmax runs
+in the library's CUDA kernels, and the host-memory (offload) entry points
+copy through the library's own streams; this module checks tensor shapes,
+allocates outputs with torch (device and pinned host memory are torch's job
+here), and passes raw pointers and the current stream through the C ABI
+declared in include/osattn.h.  If libosattn.so is missing the calls raise:
+there is no fallback implementation.
 """
 from __future__ import annotations
 
