@@ -266,17 +266,28 @@ __device__ __forceinline__ void bwd_p_part(uint32_t s_addr, int c0, float c, Vis
   tmem_ld_wait();
   reg_fence32(sa);
   reg_fence32(sb);
+  // exponent arguments s * c - LSE * log2(e) two at a time (packed fp32
+  // FMA: the same rounding as two scalar FMAs)
+  const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
   for (int g = 0; g < 16; ++g) {
     const float4 L = l2of4(c0 + 4 * g);
-    const float l2[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 4; u += 2) {
       const int x = 4 * g + u;
-      const uint32_t sv = g < 8 ? sa[x] : sb[x - 32];
-      const float e = ex2_approx(fmaf(__uint_as_float(sv), c, -l2[u]));
-      if constexpr (kMask) pr[x] = vis(c0 + x) ? e : 0.f;
-      else pr[x] = e;
+      const uint32_t s0 = g < 8 ? sa[x] : sb[x - 32], s1 = g < 8 ? sa[x + 1] : sb[x + 1 - 32];
+      const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), c2,
+                                 u == 0 ? f2_pack(-L.x, -L.y) : f2_pack(-L.z, -L.w));
+      float a0, a1;
+      f2_unpack(a2, a0, a1);
+      const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+      if constexpr (kMask) {
+        pr[x] = vis(c0 + x) ? e0 : 0.f;
+        pr[x + 1] = vis(c0 + x + 1) ? e1 : 0.f;
+      } else {
+        pr[x] = e0;
+        pr[x + 1] = e1;
+      }
     }
   }
   if constexpr (kWriteP) {
@@ -307,11 +318,15 @@ __device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& dof
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       const float4 D = dof4(c0 + 32 * ch + 4 * g);
-      const float dd[4] = {D.x, D.y, D.z, D.w};
+      const int x = 32 * ch + 4 * g;
+      // dS = P (dP - D), two at a time (packed fp32: same rounding as scalar)
+      const uint64_t d01 = f2_add(f2_pack(__uint_as_float(dv[4 * g]), __uint_as_float(dv[4 * g + 1])),
+                                  f2_pack(-D.x, -D.y));
+      const uint64_t d23 = f2_add(f2_pack(__uint_as_float(dv[4 * g + 2]), __uint_as_float(dv[4 * g + 3])),
+                                  f2_pack(-D.z, -D.w));
       float gr[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        gr[u] = pr[32 * ch + 4 * g + u] * (__uint_as_float(dv[4 * g + u]) - dd[u]);
+      f2_unpack(f2_mul(f2_pack(pr[x], pr[x + 1]), d01), gr[0], gr[1]);
+      f2_unpack(f2_mul(f2_pack(pr[x + 2], pr[x + 3]), d23), gr[2], gr[3]);
       gk[2 * g] = pack2<kF16>(gr[0], gr[1]);
       gk[2 * g + 1] = pack2<kF16>(gr[2], gr[3]);
     }
