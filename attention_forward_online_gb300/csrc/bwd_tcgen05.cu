@@ -254,76 +254,83 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O
 // results take 16-element steps 0-3 from columns 0-31 and 4-7 from 64-95.
 
 // P part over the 64 columns of this thread's group at tile column c0:
-// pr[x] = P of column c0 + x; kMask applies vis(column), l2of4(column)
-// gives LSE * log2(e) of 4 columns.  With kWriteP the 16-bit P is written
+// pr[x] = P of column c0 + x; kMask applies vis(column), nl2of4(column)
+// gives -LSE * log2(e) of 4 columns (stored negated, so the exponent
+// argument is one FMA).  With kWriteP the 16-bit P is written
 // over columns c0 .. c0 + 31.
 template <bool kF16, bool kWriteP, bool kMask, typename Vis, typename L2of4>
 __device__ __forceinline__ void bwd_p_part(uint32_t s_addr, int c0, float c, Vis&& vis,
-                                           L2of4&& l2of4, float (&pr)[64]) {
+                                           L2of4&& nl2of4, float (&pr)[64]) {
   uint32_t sa[32], sb[32];
   tmem_ld_32x32b_x32(s_addr + c0, sa);
-  tmem_ld_32x32b_x32(s_addr + c0 + 32, sb);
   tmem_ld_wait();
   reg_fence32(sa);
-  reg_fence32(sb);
-  // exponent arguments s * c - LSE * log2(e) two at a time (packed fp32
-  // FMA: the same rounding as two scalar FMAs)
+  // the second half's load lands while the first half is computed
+  tmem_ld_32x32b_x32(s_addr + c0 + 32, sb);
   const uint64_t c2 = f2_pack(c, c);
+  // Half h: columns c0 + 32h .. + 31 from sv; exponent arguments
+  // s * c - LSE * log2(e) two at a time (packed fp32 FMA: the same rounding
+  // as two scalar FMAs).  With kWriteP its 16-bit P goes over columns
+  // c0 + 16h .. + 15, which only the first half's load covered.
+  auto half = [&](const uint32_t(&sv)[32], int h) {
 #pragma unroll
-  for (int g = 0; g < 16; ++g) {
-    const float4 L = l2of4(c0 + 4 * g);
+    for (int g = 0; g < 8; ++g) {
+      const float4 L = nl2of4(c0 + 32 * h + 4 * g);
 #pragma unroll
-    for (int u = 0; u < 4; u += 2) {
-      const int x = 4 * g + u;
-      const uint32_t s0 = g < 8 ? sa[x] : sb[x - 32], s1 = g < 8 ? sa[x + 1] : sb[x + 1 - 32];
-      const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), c2,
-                                 u == 0 ? f2_pack(-L.x, -L.y) : f2_pack(-L.z, -L.w));
-      float a0, a1;
-      f2_unpack(a2, a0, a1);
-      const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
-      if constexpr (kMask) {
-        pr[x] = vis(c0 + x) ? e0 : 0.f;
-        pr[x + 1] = vis(c0 + x + 1) ? e1 : 0.f;
-      } else {
-        pr[x] = e0;
-        pr[x + 1] = e1;
+      for (int u = 0; u < 4; u += 2) {
+        const int x = 32 * h + 4 * g + u;
+        const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(sv[4 * g + u]), __uint_as_float(sv[4 * g + u + 1])), c2,
+                                   u == 0 ? f2_pack(L.x, L.y) : f2_pack(L.z, L.w));
+        float a0, a1;
+        f2_unpack(a2, a0, a1);
+        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+        if constexpr (kMask) {
+          pr[x] = vis(c0 + x) ? e0 : 0.f;
+          pr[x + 1] = vis(c0 + x + 1) ? e1 : 0.f;
+        } else {
+          pr[x] = e0;
+          pr[x + 1] = e1;
+        }
       }
     }
-  }
-  if constexpr (kWriteP) {
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
+    if constexpr (kWriteP) {
       uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack2<kF16>(pr[32 * ch + 2 * e], pr[32 * ch + 2 * e + 1]);
-      tmem_st_32x32b_x16(s_addr + c0 + 16 * ch, pk);
+      for (int e = 0; e < 16; ++e) pk[e] = pack2<kF16>(pr[32 * h + 2 * e], pr[32 * h + 2 * e + 1]);
+      tmem_st_32x32b_x16(s_addr + c0 + 16 * h, pk);
     }
-  }
+  };
+  half(sa, 0);
+  tmem_ld_wait();
+  reg_fence32(sb);
+  half(sb, 1);
 }
 
 // dS part over the same 64 columns of the dP tile at dp_addr, written as
-// 16-bit pairs over columns c0 .. c0 + 31; dof4(column) gives D of 4
-// columns.  Chunk ch reads columns c0 + 32ch .. + 31 and writes
-// c0 + 16ch .. + 15, which only earlier reads of this thread covered.
+// 16-bit pairs over columns c0 .. c0 + 31; ndof4(column) gives -D of 4
+// columns (stored negated: dP - D is one add).  Chunk ch reads columns
+// c0 + 32ch .. + 31 and writes c0 + 16ch .. + 15, which only the first
+// chunk's load covered.
 template <bool kF16, typename Dof4>
-__device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& dof4,
+__device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& ndof4,
                                             const float (&pr)[64]) {
-#pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
-    uint32_t dv[32];
-    tmem_ld_32x32b_x32(dp_addr + c0 + 32 * ch, dv);
-    tmem_ld_wait();
-    reg_fence32(dv);
+  uint32_t dva[32], dvb[32];
+  tmem_ld_32x32b_x32(dp_addr + c0, dva);
+  tmem_ld_wait();
+  reg_fence32(dva);
+  // the second chunk's load lands while the first is computed
+  tmem_ld_32x32b_x32(dp_addr + c0 + 32, dvb);
+  auto chunk = [&](const uint32_t(&dv)[32], int ch) {
     uint32_t gk[16];
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-      const float4 D = dof4(c0 + 32 * ch + 4 * g);
+      const float4 D = ndof4(c0 + 32 * ch + 4 * g);
       const int x = 32 * ch + 4 * g;
       // dS = P (dP - D), two at a time (packed fp32: same rounding as scalar)
       const uint64_t d01 = f2_add(f2_pack(__uint_as_float(dv[4 * g]), __uint_as_float(dv[4 * g + 1])),
-                                  f2_pack(-D.x, -D.y));
+                                  f2_pack(D.x, D.y));
       const uint64_t d23 = f2_add(f2_pack(__uint_as_float(dv[4 * g + 2]), __uint_as_float(dv[4 * g + 3])),
-                                  f2_pack(-D.z, -D.w));
+                                  f2_pack(D.z, D.w));
       float gr[4];
       f2_unpack(f2_mul(f2_pack(pr[x], pr[x + 1]), d01), gr[0], gr[1]);
       f2_unpack(f2_mul(f2_pack(pr[x + 2], pr[x + 3]), d23), gr[2], gr[3]);
@@ -331,7 +338,11 @@ __device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& dof
       gk[2 * g + 1] = pack2<kF16>(gr[2], gr[3]);
     }
     tmem_st_32x32b_x16(dp_addr + c0 + 16 * ch, gk);
-  }
+  };
+  chunk(dva, 0);
+  tmem_ld_wait();
+  reg_fence32(dvb);
+  chunk(dvb, 1);
 }
 
 // D (128 x N fp32) (+)= A B over 128 inner elements: A the 16-bit operand
@@ -361,8 +372,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kTileBytes;
   uint8_t* ring = smem + 2 * C::kTileBytes;  // stage s: Q_i at +0, dO_i at +kTileBytes
-  float* lse2 = reinterpret_cast<float*>(smem + C::kDkdvLse);  // [stage][query]: LSE * log2(e)
-  float* dsum = lse2 + C::kStages * kT;                        //   and D (+inf, 0 past Nq)
+  float* lse2 = reinterpret_cast<float*>(smem + C::kDkdvLse);  // [stage][query]: -LSE * log2(e)
+  float* dsum = lse2 + C::kStages * kT;                        //   and -D (-inf, 0 past Nq)
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kDkdvRegion);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -426,12 +437,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int r = 0; r < kT / 32; ++r) {
           const int q = q0 + lane + 32 * r;
-          l2[r] = INFINITY;
+          l2[r] = -INFINITY;  // staged negated: -LSE * log2(e) and -D
           dd[r] = 0.f;
           if (q < p.Nq) {
             const float L = p.LSE[rowbase + q];
-            l2[r] = (L == -INFINITY) ? INFINITY : L * kLog2e;
-            dd[r] = p.D[rowbase + q];
+            l2[r] = (L == -INFINITY) ? -INFINITY : -(L * kLog2e);
+            dd[r] = -p.D[rowbase + q];
           }
         }
         uint8_t* st = ring + s * C::kStageBytes;
@@ -757,11 +768,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q = q0 + row;
     const bool row_live = q < p.Nq;
     const long long rix = static_cast<long long>(bh) * p.Nq + q;
-    float l2 = INFINITY, Dq = 0.f;
+    float l2 = -INFINITY, Dq = 0.f;  // negated: -LSE * log2(e) and -D
     if (row_live && n_kt > 0) {
       const float L = p.LSE[rix];
-      l2 = (L == -INFINITY) ? INFINITY : L * kLog2e;
-      Dq = p.D[rix];
+      l2 = (L == -INFINITY) ? -INFINITY : -(L * kLog2e);
+      Dq = -p.D[rix];
     }
     const float4 l2v = make_float4(l2, l2, l2, l2), dv4 = make_float4(Dq, Dq, Dq, Dq);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
