@@ -279,8 +279,9 @@ __device__ __forceinline__ void bwd_p_part(uint32_t s_addr, int c0, float c, Vis
 #pragma unroll
       for (int u = 0; u < 4; u += 2) {
         const int x = 32 * h + 4 * g + u;
-        const uint64_t a2 = f2_fma(f2_pack(__uint_as_float(sv[4 * g + u]), __uint_as_float(sv[4 * g + u + 1])), c2,
-                                   u == 0 ? f2_pack(L.x, L.y) : f2_pack(L.z, L.w));
+        const uint64_t s2 =
+            f2_pack(__uint_as_float(sv[4 * g + u]), __uint_as_float(sv[4 * g + u + 1]));
+        const uint64_t a2 = f2_fma(s2, c2, u == 0 ? f2_pack(L.x, L.y) : f2_pack(L.z, L.w));
         float a0, a1;
         f2_unpack(a2, a0, a1);
         const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
@@ -327,10 +328,10 @@ __device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& ndo
       const float4 D = ndof4(c0 + 32 * ch + 4 * g);
       const int x = 32 * ch + 4 * g;
       // dS = P (dP - D), two at a time (packed fp32: same rounding as scalar)
-      const uint64_t d01 = f2_add(f2_pack(__uint_as_float(dv[4 * g]), __uint_as_float(dv[4 * g + 1])),
-                                  f2_pack(D.x, D.y));
-      const uint64_t d23 = f2_add(f2_pack(__uint_as_float(dv[4 * g + 2]), __uint_as_float(dv[4 * g + 3])),
-                                  f2_pack(D.z, D.w));
+      const uint64_t d01 = f2_add(
+          f2_pack(__uint_as_float(dv[4 * g]), __uint_as_float(dv[4 * g + 1])), f2_pack(D.x, D.y));
+      const uint64_t d23 = f2_add(
+          f2_pack(__uint_as_float(dv[4 * g + 2]), __uint_as_float(dv[4 * g + 3])), f2_pack(D.z, D.w));
       float gr[4];
       f2_unpack(f2_mul(f2_pack(pr[x], pr[x + 1]), d01), gr[0], gr[1]);
       f2_unpack(f2_mul(f2_pack(pr[x + 2], pr[x + 3]), d23), gr[2], gr[3]);
