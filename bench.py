@@ -97,10 +97,14 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # Raw nvidia-smi samples of the timed region go to this directory (under
+    # the repository, git-ignored); OSATTN_CLOCKS_DIR overrides it.
+    LOG_DIR = os.environ.get("OSATTN_CLOCKS_DIR", os.path.join(ROOT, "bench_logs"))
+
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_gpu{gpu_index}.csv")
+        self.path = os.path.join(self.LOG_DIR, f"clocks_bench_gpu{gpu_index}.csv")
 
     def start(self):
         try:
