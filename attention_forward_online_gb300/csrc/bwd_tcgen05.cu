@@ -12,7 +12,7 @@
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j.
 //
 // Three launches on one stream:
-//   bwd_rowdot_kernel  D = rowsum(dO * O) in fp32 (HBM-bound, one warp a row).
+//   bwd_rowdot_kernel  D = rowsum(dO * O) in fp32 (HBM-bound, 16-byte loads).
 //   bwd_dkdv_kernel    one CTA per 128-key tile of a (b, h): K and V stay in
 //                      shared memory while the query tiles that can see
 //                      those keys stream through a TMA ring.  Per query tile:
@@ -200,46 +200,73 @@ __device__ __forceinline__ void write_row(uint16_t* dst, uint32_t taddr, bool ha
 }
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
-template <typename T>
-__device__ __forceinline__ float2 load2(const T* p);
-template <>
-__device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
-template <>
-__device__ __forceinline__ float2 load2<__half>(const __half* p) {
-  return __half22float2(*reinterpret_cast<const __half2*>(p));
-}
-template <>
-__device__ __forceinline__ float2 load2<float>(const float* p) {
-  return *reinterpret_cast<const float2*>(p);
-}
-
 struct RowStrides {
   long long o[3], g[3];  // element strides of the b, h and row axes of O and dO
 };
 
+// Two 16-bit values packed in one 32-bit word, as floats.
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const T* __restrict__ O,
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// D = rowsum(dO * O) in fp32.  A row is d * sizeof(T) / 16 16-byte
+// vectors, read by that many consecutive lanes (every row starts 16-byte
+// aligned: the entry points require 16-byte aligned bases and strides), so
+// a warp covers several rows per pass; each warp issues the loads of
+// kPasses passes before using any, to keep enough bytes in flight for the
+// HBM stream.  The lanes of a row sum their partial dots by shuffles.
+template <typename T>
+__global__ void __launch_bounds__(256, 3) bwd_rowdot_kernel(const T* __restrict__ O,
                                                          const T* __restrict__ dO,
                                                          float* __restrict__ D, long long rows,
                                                          int d, int H, int Nq, RowStrides st) {
+  constexpr int kPasses = 4;
+  constexpr int kEpv = 16 / static_cast<int>(sizeof(T));  // elements per vector
   const int lane = threadIdx.x & 31;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       row < rows; row += warps) {
-    const long long bh = row / Nq;
-    const long long i = row - bh * Nq, b = bh / H, h = bh - b * H;
-    const T* o = O + b * st.o[0] + h * st.o[1] + i * st.o[2];
-    const T* g = dO + b * st.g[0] + h * st.g[1] + i * st.g[2];
-    float acc = 0.f;
-    for (int c = 2 * lane; c < d; c += 64) {
-      const float2 a = load2<T>(o + c), b = load2<T>(g + c);
-      acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+  const int lpr = d / kEpv;                 // lanes per row
+  const int rpw = 32 / lpr;                 // rows per warp pass
+  const int sub = lane / lpr, vec = lane - sub * lpr;
+  const long long warp = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long step = static_cast<long long>(gridDim.x) * (blockDim.x >> 5) * rpw * kPasses;
+  for (long long base = warp * rpw * kPasses; base < rows; base += step) {
+    uint4 a[kPasses], g[kPasses];
+#pragma unroll
+    for (int u = 0; u < kPasses; ++u) {
+      const long long row = base + u * rpw + sub;
+      a[u] = make_uint4(0u, 0u, 0u, 0u);
+      g[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < rows) {
+        const long long bh = row / Nq;
+        const long long i = row - bh * Nq, b = bh / H, h = bh - b * H;
+        a[u] = reinterpret_cast<const uint4*>(O + b * st.o[0] + h * st.o[1] + i * st.o[2])[vec];
+        g[u] = reinterpret_cast<const uint4*>(dO + b * st.g[0] + h * st.g[1] + i * st.g[2])[vec];
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) D[row] = acc;
+    for (int u = 0; u < kPasses; ++u) {
+      const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+      const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (sizeof(T) == 4) {
+          acc = fmaf(__uint_as_float(aw[e]), __uint_as_float(gw[e]), acc);
+        } else {
+          const float2 x = unpack2<T>(aw[e]), y = unpack2<T>(gw[e]);
+          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+      }
+      for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long row = base + u * rpw + sub;
+      if (vec == 0 && row < rows) D[row] = acc;
+    }
   }
 }
 
@@ -841,8 +868,13 @@ cudaError_t set_bwd_attrs() {
 template <typename T>
 cudaError_t launch_rowdot(const BwdArgs& a) {
   const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
-  const long long want = static_cast<long long>(a.num_sms) * 16;
-  const int rgrid = static_cast<int>((rows + 7) / 8 < want ? (rows + 7) / 8 : want);
+  // 8 warps a block, each taking 4 passes of 32 / (lanes per row) rows at
+  // a time; 3 blocks per SM, all resident at once
+  const long long lanes_per_row = static_cast<long long>(a.d) * sizeof(T) / 16;
+  const long long per_block = 8ll * 4 * (32 / lanes_per_row);
+  const long long want = static_cast<long long>(a.num_sms) * 3;
+  const long long need = (rows + per_block - 1) / per_block;
+  const int rgrid = static_cast<int>(need < want ? need : want);
   RowStrides rs;
   for (int i = 0; i < 3; ++i) {
     rs.o[i] = a.o_strides[i];
