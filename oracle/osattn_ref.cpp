@@ -390,59 +390,108 @@ int osattn_ref_attention_blocked(const void* Q, const void* K, const void* V, in
 //   dS_ij = P_ij (dP_ij - D_i)               (softmax Jacobian)
 //   dQ_i  = scale * sum_j dS_ij K_j
 //   dK_j  = scale * sum_i dS_ij Q_i
+// Two passes, each parallel over rows so that whole heads of long sequences
+// can be checked:
+//   pass 1, one task per query row i: s_ij, LSE_i, P_ij, dP_ij, D_i and dQ_i;
+//           LSE_i and D_i are kept;
+//   pass 2, one task per key row j: for every query row i whose J_i holds j,
+//           s_ij, P_ij = exp(s_ij - LSE_i), dP_ij and dS_ij again, summed
+//           into dK_j and dV_j.
 // A row with J empty contributes nothing.  dQ [B,H,Nq,d], dK and dV
-// [B,H,Nkv,d], all double.  One thread per (b, h).
-// Returns 0, or 1 for an invalid argument (nothing written).
+// [B,H,Nkv,d], all double.  Returns 0, or 1 for an invalid argument
+// (nothing written).
 int osattn_ref_attention_bwd(const void* Q, const void* K, const void* V, const void* dO,
                              int dtype, double* dQ, double* dK, double* dV, int B, int H, int Nq,
                              int Nkv, int d, double scale, int causal, const int32_t* key_len,
                              int nthreads) {
   AttnProblem p{Q, K, V, dtype, B, H, Nq, Nkv, d, scale, causal, key_len};
   if (check_problem(p) || !dO || !dQ || !dK || !dV) return 1;
+  // The inputs widened to double once (exact, as in load_elem).
+  const int64_t nq = static_cast<int64_t>(B) * H * Nq * d;
+  const int64_t nk = static_cast<int64_t>(B) * H * Nkv * d;
+  std::vector<double> q(nq), g(nq), k(nk), v(nk);
   parallel_rows(static_cast<int64_t>(B) * H, nthreads, [&](int64_t bh) {
-    const int b = static_cast<int>(bh / H);
-    const int64_t qbase = bh * static_cast<int64_t>(Nq) * d;
-    const int64_t kbase = bh * static_cast<int64_t>(Nkv) * d;
-    for (int64_t e = 0; e < static_cast<int64_t>(Nkv) * d; ++e) {
-      dK[kbase + e] = 0.0;
-      dV[kbase + e] = 0.0;
+    for (int64_t e = bh * Nq * d; e < (bh + 1) * Nq * d; ++e) {
+      q[e] = load_elem(Q, dtype, e);
+      g[e] = load_elem(dO, dtype, e);
     }
-    std::vector<double> s(Nkv), pr(Nkv), dp(Nkv);
-    for (int i = 0; i < Nq; ++i) {
-      double* dq = dQ + qbase + static_cast<int64_t>(i) * d;
-      for (int c = 0; c < d; ++c) dq[c] = 0.0;
-      int jend = visible_keys(p, b);
-      if (causal) jend = std::min(jend, i + 1);
-      if (jend <= 0) continue;
-      const int64_t qoff = qbase + static_cast<int64_t>(i) * d;
-      for (int j = 0; j < jend; ++j) {
-        double acc = 0.0;
-        for (int k = 0; k < d; ++k)
-          acc += load_elem(Q, dtype, qoff + k) * load_elem(K, dtype, kbase + static_cast<int64_t>(j) * d + k);
-        s[j] = scale * acc;
-      }
-      double m = kNegInf;
-      for (int j = 0; j < jend; ++j) m = std::max(m, s[j]);
-      double den = 0.0;
-      for (int j = 0; j < jend; ++j) den += std::exp(s[j] - m);
-      const double lse = m + std::log(den);
-      double D = 0.0;
-      for (int j = 0; j < jend; ++j) {
-        pr[j] = std::exp(s[j] - lse);
-        double acc = 0.0;
-        for (int c = 0; c < d; ++c)
-          acc += load_elem(dO, dtype, qoff + c) * load_elem(V, dtype, kbase + static_cast<int64_t>(j) * d + c);
-        dp[j] = acc;
-        D += pr[j] * dp[j];
-      }
-      for (int j = 0; j < jend; ++j) {
-        const double ds = pr[j] * (dp[j] - D);
-        const int64_t koff = kbase + static_cast<int64_t>(j) * d;
-        for (int c = 0; c < d; ++c) {
-          dq[c] += scale * ds * load_elem(K, dtype, koff + c);
-          dK[koff + c] += scale * ds * load_elem(Q, dtype, qoff + c);
-          dV[koff + c] += pr[j] * load_elem(dO, dtype, qoff + c);
-        }
+    for (int64_t e = bh * Nkv * d; e < (bh + 1) * Nkv * d; ++e) {
+      k[e] = load_elem(K, dtype, e);
+      v[e] = load_elem(V, dtype, e);
+    }
+  });
+  auto dot = [d](const double* a, const double* b) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += a[c] * b[c];
+    return acc;
+  };
+  std::vector<double> row_lse(static_cast<int64_t>(B) * H * Nq), row_D(row_lse.size());
+
+  // pass 1: query rows
+  parallel_rows(static_cast<int64_t>(B) * H * Nq, nthreads, [&](int64_t r) {
+    const int64_t bh = r / Nq;
+    const int i = static_cast<int>(r % Nq);
+    const int b = static_cast<int>(bh / H);
+    const double* qi = q.data() + r * d;
+    const double* gi = g.data() + r * d;
+    const double* kb = k.data() + bh * Nkv * d;
+    const double* vb = v.data() + bh * Nkv * d;
+    double* dq = dQ + r * d;
+    for (int c = 0; c < d; ++c) dq[c] = 0.0;
+    int jend = visible_keys(p, b);
+    if (causal) jend = std::min(jend, i + 1);
+    row_lse[r] = kNegInf;
+    row_D[r] = 0.0;
+    if (jend <= 0) return;
+    thread_local std::vector<double> s, pr, dp;
+    s.resize(Nkv);
+    pr.resize(Nkv);
+    dp.resize(Nkv);
+    for (int j = 0; j < jend; ++j) s[j] = scale * dot(qi, kb + static_cast<int64_t>(j) * d);
+    double m = kNegInf;
+    for (int j = 0; j < jend; ++j) m = std::max(m, s[j]);
+    double den = 0.0;
+    for (int j = 0; j < jend; ++j) den += std::exp(s[j] - m);
+    const double lse = m + std::log(den);
+    double D = 0.0;
+    for (int j = 0; j < jend; ++j) {
+      pr[j] = std::exp(s[j] - lse);
+      dp[j] = dot(gi, vb + static_cast<int64_t>(j) * d);
+      D += pr[j] * dp[j];
+    }
+    for (int j = 0; j < jend; ++j) {
+      const double ds = pr[j] * (dp[j] - D);
+      const double* kj = kb + static_cast<int64_t>(j) * d;
+      for (int c = 0; c < d; ++c) dq[c] += scale * ds * kj[c];
+    }
+    row_lse[r] = lse;
+    row_D[r] = D;
+  });
+
+  // pass 2: key rows
+  parallel_rows(static_cast<int64_t>(B) * H * Nkv, nthreads, [&](int64_t r) {
+    const int64_t bh = r / Nkv;
+    const int j = static_cast<int>(r % Nkv);
+    const int b = static_cast<int>(bh / H);
+    const double* kj = k.data() + r * d;
+    const double* vj = v.data() + r * d;
+    double* dk = dK + r * d;
+    double* dv = dV + r * d;
+    for (int c = 0; c < d; ++c) {
+      dk[c] = 0.0;
+      dv[c] = 0.0;
+    }
+    if (j >= visible_keys(p, b)) return;  // no row sees key j
+    const int i0 = causal ? j : 0;        // rows i with j <= i
+    for (int i = i0; i < Nq; ++i) {
+      const int64_t qr = bh * Nq + i;
+      const double* qi = q.data() + qr * d;
+      const double* gi = g.data() + qr * d;
+      const double pij = std::exp(scale * dot(qi, kj) - row_lse[qr]);
+      const double dsij = pij * (dot(gi, vj) - row_D[qr]);
+      for (int c = 0; c < d; ++c) {
+        dk[c] += scale * dsij * qi[c];
+        dv[c] += pij * gi[c];
       }
     }
   });

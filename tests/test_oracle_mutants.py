@@ -38,12 +38,15 @@ MUTANTS = {
                              "mag = std::ldexp(static_cast<double>(1024 + f), -25);"),
     "bwd_drops_row_term": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * dp[j];"),
     "bwd_sign": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * (D - dp[j]);"),
-    "bwd_dk_without_scale": ("dK[koff + c] += scale * ds * load_elem(Q, dtype, qoff + c);",
-                             "dK[koff + c] += ds * load_elem(Q, dtype, qoff + c);"),
-    "bwd_dv_wrong_operand": ("dV[koff + c] += pr[j] * load_elem(dO, dtype, qoff + c);",
-                             "dV[koff + c] += pr[j] * load_elem(Q, dtype, qoff + c);"),
-    "bwd_dq_transposed_key": ("dq[c] += scale * ds * load_elem(K, dtype, koff + c);",
-                              "dq[c] += scale * ds * load_elem(K, dtype, kbase + static_cast<int64_t>(c % Nkv) * d + j % d);"),
+    "bwd_dq_transposed_key": ("for (int c = 0; c < d; ++c) dq[c] += scale * ds * kj[c];",
+                              "for (int c = 0; c < d; ++c) dq[c] += scale * ds * kb[(c % Nkv) * d + j % d];"),
+    "bwd_keyrow_drops_row_term": ("const double dsij = pij * (dot(gi, vj) - row_D[qr]);",
+                                  "const double dsij = pij * dot(gi, vj);"),
+    "bwd_keyrow_without_lse": ("const double pij = std::exp(scale * dot(qi, kj) - row_lse[qr]);",
+                               "const double pij = std::exp(scale * dot(qi, kj));"),
+    "bwd_keyrow_causal_off_by_one": ("const int i0 = causal ? j : 0;", "const int i0 = causal ? j + 1 : 0;"),
+    "bwd_dk_without_scale": ("dk[c] += scale * dsij * qi[c];", "dk[c] += dsij * qi[c];"),
+    "bwd_dv_wrong_operand": ("dv[c] += pij * gi[c];", "dv[c] += pij * qi[c];"),
 }
 
 
