@@ -1,24 +1,19 @@
 """GPU parity of the backward pass (osattn_bwd: dQ, dK, dV) against the fp64
 oracle's gradients, on the forward outputs (O, LSE) of the library itself.
 
-Gate per gradient tensor g (reading c18):
-    |g - g_ref| <= 2e-2 |g_ref| + t * rms(g_ref) + half an ulp of g_ref + 1e-5,
-with t = 8e-2 for bf16 and 1.5e-2 for fp16.  fp32 (SIMT kernels, fp32
-throughout) is gated by |g - g_ref| <= 1e-4 |g_ref| + 1e-4 rms(g_ref) + 1e-6:
-its only departures from exact arithmetic are fp32 roundings, and the
-largest of them, a d-term score dot product (relative error below
+16-bit gates per gradient tensor g (reading c18), from the rounding model in
+tests/_bwd_model.py, which tests/test_bwd_rounding_model.py checks on the
+CPU:
+    elementwise  |g - g_ref| <= t_max rms(g_ref) + half an ulp of g_ref + 1e-5
+    aggregate    rms(g - g_ref) <= t_rms rms(g_ref)
+with (t_max, t_rms) per tensor 1.5 times what the model of the kernels'
+roundings (P and dS to 16 bits, D from the stored 16-bit O, the forward's
+16-bit P and O) predicts on the very cases below.  fp32 (SIMT kernels,
+fp32 throughout) is gated by |g - g_ref| <= 1e-4 |g_ref| + 1e-4 rms(g_ref)
++ 1e-6: its only departures from exact arithmetic are fp32 roundings, and
+the largest of them, a d-term score dot product (relative error below
 d * 2^-24 of sum |q_k k_k|, about 8e-5 in the exponent for d = 128 and the
-inputs below), bounds the relative error of P and hence of each gradient.  The kernels round P and dS to
-the input type before the MMAs (unit roundoff u = 2^-9 for bf16, 2^-12 for
-fp16), read D from the 16-bit O of the forward pass, accumulate in fp32 and
-round the result once more.  Each row of dS sums to zero, so dQ and dK are
-cancellations whose rounding error is a fraction of the gradient's rms
-rather than of the element: an fp64 model of exactly these roundings puts
-the largest error at 5.3 % of rms for bf16 and 0.84 % for fp16 on the cases
-below, and t is 1.5 times that.  The 1e-5 floor covers gradients that are
-exactly zero (a single visible key): there dP and D are the same d-term dot
-product summed in two different fp32 orders, whose difference (about
-d * 2^-24 for unit-scale inputs) becomes a tiny nonzero dS.
+inputs below), bounds the relative error of P and hence of each gradient.
 """
 import math
 
@@ -26,29 +21,24 @@ import numpy as np
 import pytest
 import torch
 
+import _bwd_model as M
 import oracle
 from attention_forward_online_gb300 import osattn
 from attention_forward_online_gb300.inputs import make_qkv
-
-from _compare import half_ulp_bf16, half_ulp_fp16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 KIND = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
 
 
-T_RMS = {"bf16": 8e-2, "fp16": 1.5e-2, "fp32": 1e-4}
-
-
-def check_grad(g, ref, kind, name):
+def check_grad(g, ref, kind, name, gates=None):
     g = np.asarray(g, dtype=np.float64)
+    if kind != "fp32":
+        gates = gates or M.GATES["small"][kind]
+        return M.check_grad_gate(g, ref, gates[name], kind, name)
     assert not np.isnan(g).any(), f"NaN in {name}"
     rms = math.sqrt(float((ref ** 2).mean())) if ref.size else 0.0
-    if kind == "fp32":
-        gate = 1e-4 * np.abs(ref) + T_RMS[kind] * rms + 1e-6
-    else:
-        ulp = half_ulp_bf16(ref) if kind == "bf16" else half_ulp_fp16(ref)
-        gate = 2e-2 * np.abs(ref) + T_RMS[kind] * rms + ulp + 1e-5
+    gate = 1e-4 * np.abs(ref) + 1e-4 * rms + 1e-6
     err = np.abs(g - ref)
     bad = err > gate
     assert not bad.any(), (f"{name}: error {err.max():.3e} over gate at {np.argwhere(bad)[:4].tolist()} "
@@ -57,9 +47,7 @@ def check_grad(g, ref, kind, name):
 
 
 def run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed):
-    q, k, v = make_qkv(B, H, Nq, Nkv, d, dtype, seed=seed, q_std=1.5)
-    g = torch.Generator().manual_seed(seed + 1)
-    do = torch.randn(B, H, Nq, d, generator=g).to(dtype)
+    q, k, v, do = M.small_case_inputs((B, H, Nq, Nkv, d, causal, kl), dtype, seed)
     qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
     kld = None if kl is None else torch.tensor(kl, dtype=torch.int32, device=DEV)
     scale = 1 / math.sqrt(d)
@@ -76,25 +64,15 @@ def run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed):
     return stats, (dq, dk, dv)
 
 
-CASES = [
-    # B, H, Nq, Nkv, d, causal, key_len
-    (1, 1, 128, 128, 64, False, None),
-    (1, 2, 256, 256, 128, True, None),
-    (2, 2, 200, 333, 64, False, [333, 100]),
-    (1, 1, 130, 300, 128, True, None),
-    (1, 1, 300, 130, 64, True, None),
-    (1, 1, 1, 1, 64, False, None),
-    (2, 1, 257, 257, 128, True, [257, 129]),
-    (1, 2, 384, 512, 128, False, [400]),
-]
+CASES = M.SMALL_CASES  # B, H, Nq, Nkv, d, causal, key_len
 
 
 @pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else "") + f"kl{c[6]}")
 def test_bwd_matches_oracle(case, dtype):
     B, H, Nq, Nkv, d, causal, kl = case
-    stats, _ = run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed=4000 + Nq + Nkv + d)
-    print(case, KIND[dtype], "max err / rms (dQ, dK, dV):", stats)
+    stats, _ = run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed=M.small_case_seed(case))
+    print(case, KIND[dtype], "(max err, rms err) / rms (dQ, dK, dV):", stats)
 
 
 def test_bwd_fully_masked_batch_has_zero_gradients():
@@ -113,10 +91,9 @@ def test_bwd_fully_masked_batch_has_zero_gradients():
 
 
 def test_bwd_deterministic():
-    stats, (dq1, dk1, dv1) = run_case(1, 4, 512, 512, 128, True, None, torch.bfloat16, seed=91)
-    q, k, v = make_qkv(1, 4, 512, 512, 128, torch.bfloat16, seed=91, q_std=1.5)
-    g = torch.Generator().manual_seed(92)
-    do = torch.randn(1, 4, 512, 128, generator=g).to(torch.bfloat16)
+    B, H, Nq, Nkv, d, causal, kl = M.DETERMINISM_CASE
+    stats, (dq1, dk1, dv1) = run_case(B, H, Nq, Nkv, d, causal, kl, torch.bfloat16, seed=91)
+    q, k, v, do = M.small_case_inputs(M.DETERMINISM_CASE, torch.bfloat16, 91)
     qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
     o, lse = osattn.fwd(qd, kd, vd, causal=True)
     dq2, dk2, dv2 = osattn.bwd(qd, kd, vd, o, lse, dod, causal=True)
@@ -125,33 +102,27 @@ def test_bwd_deterministic():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_bwd_full_size_workloads_sampled_heads():
+@pytest.mark.parametrize("name", M.FULL_SIZE)
+def test_bwd_full_size_workloads_whole_heads(name):
     # The backward workloads at full size, in the launch configuration the
-    # bench times: whole heads of the B8 H40 2048 d128 problem against the
-    # oracle; for the causal 16K problem, dQ of the first 2048 query rows (a
-    # causal row only depends on keys up to its own index, so a prefix of the
-    # problem has the same dQ rows) and finiteness everywhere.
+    # bench times; dQ, dK and dV of the whole last two heads against the
+    # oracle (the causal 16K rows at full length), finiteness everywhere.
     from attention_forward_online_gb300.inputs import BWD_WORKLOADS, make_grad_out, make_inputs
 
-    for name, heads, prefix in (("bwd_bf16_b8_h40_n2048_d128", 2, None),
-                                ("bwd_bf16_causal_b1_h32_n16384_d128_qstd3", 2, 2048)):
-        w = BWD_WORKLOADS[name]
-        q, k, v, _ = make_inputs(w)
-        do = make_grad_out(w)
-        qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
-        o, lse = osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal)
-        dq, dk, dv = osattn.bwd(qd, kd, vd, o, lse, dod, scale=w.scale, causal=w.causal)
-        assert osattn.get_device_status() == osattn.OK
-        for t in (dq, dk, dv):
-            assert torch.isfinite(t.float()).all().item()
-        n = prefix or w.Nq
-        sl = (slice(w.B - 1, w.B), slice(w.H - heads, w.H), slice(0, n))
-        rq, rk, rv = oracle.attention_bwd(q[sl], k[sl], v[sl], do[sl], w.scale, w.causal)
-        out = [check_grad(dq[sl].double().cpu().numpy(), rq, "bf16", "dQ")]
-        if prefix is None:
-            out.append(check_grad(dk[sl].double().cpu().numpy(), rk, "bf16", "dK"))
-            out.append(check_grad(dv[sl].double().cpu().numpy(), rv, "bf16", "dV"))
-        print(name, "max err / rms:", out)
+    w = BWD_WORKLOADS[name]
+    q, k, v, _ = make_inputs(w)
+    do = make_grad_out(w)
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
+    o, lse = osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal)
+    dq, dk, dv = osattn.bwd(qd, kd, vd, o, lse, dod, scale=w.scale, causal=w.causal)
+    assert osattn.get_device_status() == osattn.OK
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all().item()
+    sl = (slice(w.B - 1, w.B), slice(w.H - M.FULL_SIZE_HEADS, w.H))
+    ref = oracle.attention_bwd(q[sl], k[sl], v[sl], do[sl], w.scale, w.causal)
+    out = [check_grad(t[sl].double().cpu().numpy(), r, "bf16", n, M.GATES[name]["bf16"])
+           for t, r, n in zip((dq, dk, dv), ref, ("dQ", "dK", "dV"))]
+    print(name, "(max err, rms err) / rms (dQ, dK, dV):", out)
 
 
 def _bnhd(t):
@@ -160,17 +131,15 @@ def _bnhd(t):
 
 
 @pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
-@pytest.mark.parametrize("case", [(2, 3, 300, 333, 64, False, [333, 100]), (1, 2, 257, 257, 128, True, None)],
+@pytest.mark.parametrize("case", M.STRIDED_CASES,
                          ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else ""))
 def test_bwd_strided_matches_contiguous_bitwise(case, dtype):
     # Q, K, V, O, dO read and dQ, dK, dV written in the [B, N, H, d] layout
     # (osattn_bwd_strided) give the contiguous call's gradients bit for bit,
     # and therefore pass the oracle gate too.
     B, H, Nq, Nkv, d, causal, kl = case
-    stats, (dq1, dk1, dv1) = run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed=4000 + Nq + Nkv + d)
-    q, k, v = make_qkv(B, H, Nq, Nkv, d, dtype, seed=4000 + Nq + Nkv + d, q_std=1.5)
-    g = torch.Generator().manual_seed(4000 + Nq + Nkv + d + 1)
-    do = torch.randn(B, H, Nq, d, generator=g).to(dtype)
+    stats, (dq1, dk1, dv1) = run_case(B, H, Nq, Nkv, d, causal, kl, dtype, seed=M.small_case_seed(case))
+    q, k, v, do = M.small_case_inputs(case, dtype)
     qd, kd, vd, dod = (_bnhd(t.to(DEV)) for t in (q, k, v, do))
     assert not qd.is_contiguous()
     kld = None if kl is None else torch.tensor(kl, dtype=torch.int32, device=DEV)
