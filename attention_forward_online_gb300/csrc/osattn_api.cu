@@ -28,6 +28,7 @@ constexpr int kOffloadEvents = 64;  // event ring of the offload pipeline
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int row_cluster_max = 8;  // CTAs per cluster of the split-row softmax
   unsigned int* status = nullptr;  // device address of g_device_status
   // Offload pipeline (osattn_fwd_offload), created on first use: a
   // host-to-device and a device-to-host copy stream and their events.
@@ -68,6 +69,7 @@ int device_state(DeviceState** out) {
     if (osattn::prepare_fwd_bf16() != cudaSuccess) return OSATTN_ERR_CUDA;
     if (osattn::prepare_bwd() != cudaSuccess || osattn::prepare_bwd_fp32() != cudaSuccess)
       return OSATTN_ERR_CUDA;
+    if (osattn::prepare_softmax_rows(&st.row_cluster_max) != cudaSuccess) return OSATTN_ERR_CUDA;
     if (!g_encode_tiled) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -468,12 +470,27 @@ int softmax_rows_offload_impl(const void* in_h, void* out_h, float* lse_h, void*
                             const size_t off = static_cast<size_t>(r0) * rb;
                             const cudaError_t e = osattn::launch_softmax_rows(
                                 static_cast<const char*>(in) + off, static_cast<char*>(out) + off,
-                                lse ? lse + r0 : nullptr, nr, N, dtype, ds->num_sms, cs);
+                                lse ? lse + r0 : nullptr, nr, N, dtype, ds->num_sms,
+                                ds->row_cluster_max, cs);
                             return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
                           });
 }
 
 }  // namespace
+
+namespace osattn {
+
+int validate_splitkv(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                     int B, int H, int Nq, int Nkv, int d, float scale, const int32_t* key_len,
+                     int dtype, int num_splits) {
+  const int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  if (rc != OSATTN_OK) return rc;
+  if (dtype == OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
+  if (num_splits < 1 || num_splits > OSATTN_MAX_SPLITS) return OSATTN_ERR_INVALID_ARG;
+  return OSATTN_OK;
+}
+
+}  // namespace osattn
 
 extern "C" {
 
@@ -518,10 +535,9 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
                        int H, int Nq, int Nkv, int d, float scale, int causal,
                        const int32_t* key_len, int dtype, int num_splits, void* workspace,
                        size_t workspace_bytes, void* stream) {
-  int rc = validate_fwd(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype);
+  int rc = osattn::validate_splitkv(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype,
+                                    num_splits);
   if (rc != OSATTN_OK) return rc;
-  if (dtype == OSATTN_FP32) return OSATTN_ERR_UNSUPPORTED;
-  if (num_splits < 1 || num_splits > OSATTN_MAX_SPLITS) return OSATTN_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
     return OSATTN_ERR_INVALID_ARG;
@@ -659,7 +675,7 @@ int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int
   int rc = device_state(&st);
   if (rc != OSATTN_OK) return rc;
   const cudaError_t e = osattn::launch_softmax_rows(in, out, lse, static_cast<long long>(rows), N,
-                                                    dtype, st->num_sms,
+                                                    dtype, st->num_sms, st->row_cluster_max,
                                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }

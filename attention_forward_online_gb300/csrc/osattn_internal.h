@@ -46,6 +46,12 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUte
 
 // Split-KV combine (splitkv_combine.cu): folds the partials of each row with
 // the (m, l) combine and writes O (bf16) and LSE.
+// Host checks of osattn_fwd_splitkv other than its workspace (pointers,
+// sizes, alignment, scale, d, dtype, 1 <= num_splits <= OSATTN_MAX_SPLITS);
+// OSATTN_OK or the status the entry point returns.
+int validate_splitkv(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                     int B, int H, int Nq, int Nkv, int d, float scale, const int32_t* key_len,
+                     int dtype, int num_splits);
 cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, void* O,
                                    float* LSE, long long rows, int d, int num_splits, int fp16,
                                    cudaStream_t stream);
@@ -88,8 +94,11 @@ cudaError_t launch_bwd_rowdot_fp32(const BwdArgs& a);  // D for fp32 O and dO (b
 
 // Standalone row softmax (softmax_rows.cu) over a [rows, N] matrix;
 // elem: 0 bf16, 1 fp32, 2 fp16 (the public dtype codes).
+// Row softmax: per-device set-up (cluster attributes; the largest cluster,
+// 16 or 8 CTAs of 1024 threads, the GPU co-schedules) and the launch.
+cudaError_t prepare_softmax_rows(int* max_cluster);
 cudaError_t launch_softmax_rows(const void* in, void* out, float* lse, long long rows, int N,
-                                int elem, int num_sms, cudaStream_t stream);
+                                int elem, int num_sms, int max_cluster, cudaStream_t stream);
 
 // Box shape the bf16 kernel expects in its tensor maps.
 constexpr int kBoxInner = 64;   // elements along d (128 bytes)

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "osattn.h"
+#include "osattn_internal.h"
 
 namespace {
 
@@ -31,7 +32,9 @@ std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of this device's copy of the scratch array (looked up on
-// the first call for the device).  Returns OSATTN_OK or OSATTN_ERR_CUDA.
+// the first call for the device, in the runtime's primary context; a device
+// reset makes a new context whose copy may sit elsewhere, which the cache
+// does not notice).  Returns OSATTN_OK or OSATTN_ERR_CUDA.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OSATTN_ERR_CUDA;
@@ -52,11 +55,16 @@ extern "C" int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const vo
                                           float* LSE, int B, int H, int Nq, int Nkv, int d,
                                           float scale, int causal, const int32_t* key_len,
                                           int dtype, int num_splits, void* stream) {
-  // Size limit first: the partials of every (split, row) must fit the array.
+  // The arguments first (the same checks and statuses as
+  // osattn_fwd_splitkv), then whether the partials of every (split, row)
+  // fit the array.
+  int rc = osattn::validate_splitkv(Q, K, V, O, LSE, B, H, Nq, Nkv, d, scale, key_len, dtype,
+                                    num_splits);
+  if (rc != OSATTN_OK) return rc;
   const size_t need = osattn_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
   if (need > kScratchBytes) return OSATTN_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != OSATTN_OK) return rc;
   // Nothing in the scratch has to start at zero: the split kernel writes
   // every partial that the combine reads, in every call.

@@ -220,13 +220,22 @@ int osattn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, flo
  * is rejected with OSATTN_ERR_SCRATCH_LIMIT before anything is enqueued;
  * use fewer splits, or osattn_fwd_splitkv with your own workspace.
  *
+ * Arguments are checked first, with the statuses osattn_fwd_splitkv
+ * returns; OSATTN_ERR_SCRATCH_LIMIT only follows for valid arguments.
+ *
  * The call allocates nothing.  Its first call on a device looks up that
  * device's copy of the array (cudaGetSymbolAddress, with the device
- * current); make that first call before any stream capture.  Every call on
- * a device shares the one array and leaves its contents behind; nothing in
- * it has to start at zero.  Calls whose kernels can overlap on the GPU (for
- * example on two streams without ordering between them) race on the array
- * and give undefined results: order them on one stream or with events.
+ * current) and keeps the address; make that first call before any stream
+ * capture.  The address belongs to the runtime's primary context: the entry
+ * point assumes the caller uses that context and does not reset the device
+ * (cudaDeviceReset) between calls.  Every call on a device shares the one
+ * array and leaves its contents behind; a successful call writes every
+ * partial it reads, so nothing in it has to start at zero.  After
+ * osattn_get_device_status reports OSATTN_ERR_TIMEOUT, O and LSE of the
+ * calls since the last status read may hold data left in the array by
+ * earlier calls: discard them.  Calls whose kernels can overlap on the GPU
+ * (for example on two streams without ordering between them) race on the
+ * array and give undefined results: order them on one stream or with events.
  */
 int osattn_fwd_splitkv_noalloc(const void* Q, const void* K, const void* V, void* O,
                                float* LSE, int B, int H, int Nq, int Nkv, int d, float scale,

@@ -133,6 +133,28 @@ def test_noalloc_rejects_problems_beyond_its_scratch(L):
     assert "scratch" in osattn.status_string(rc)
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(splits=129), osattn.ERR_INVALID_ARG),
+    (dict(splits=0), osattn.ERR_INVALID_ARG),
+    (dict(q=None), osattn.ERR_INVALID_ARG),
+    (dict(o=P + 8), osattn.ERR_INVALID_ARG),
+    (dict(dtype=osattn.FP32), osattn.ERR_UNSUPPORTED),
+    (dict(d=96), osattn.ERR_UNSUPPORTED),
+])
+@pytest.mark.parametrize("large", [False, True], ids=["small", "beyond_scratch"])
+def test_noalloc_checks_arguments_before_its_scratch_limit(L, kw, expect, large):
+    # Invalid arguments get the statuses of osattn_fwd_splitkv whether or not
+    # the problem would also exceed the built-in scratch array.
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=4 if large else 1, H=8 if large else 1,
+             Nq=4096 if large else 8, Nkv=4096 if large else 8, d=128, dtype=osattn.BF16,
+             splits=4)
+    a.update(kw)
+    rc = L.osattn_fwd_splitkv_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                      a["Nq"], a["Nkv"], a["d"], 0.125, 0, None, a["dtype"],
+                                      a["splits"], ctypes.c_void_p(None))
+    assert rc == expect
+
+
 def test_softmax_rows_host_validation(L):
     f = L.osattn_softmax_rows
     nul = ctypes.c_void_p(None)
