@@ -137,6 +137,10 @@ ROW_WORKLOADS = {
     for w in [
         RowWorkload("softmax_rows_bf16_r65536_n4096", "bf16", 65536, 4096, seed=6),
         RowWorkload("softmax_rows_fp32_r32768_n4096", "fp32", 32768, 4096, seed=7),
+        # the chapter's closing exercise: rows of 1M elements, each split
+        # across the CTAs of a thread-block cluster
+        RowWorkload("softmax_rows_bf16_r256_n1048576", "bf16", 256, 1 << 20, seed=8),
+        RowWorkload("softmax_rows_fp32_r128_n1048576", "fp32", 128, 1 << 20, seed=9),
     ]
 }
 

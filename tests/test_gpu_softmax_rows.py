@@ -15,7 +15,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 SHAPES = [(7, 1), (5, 3), (33, 8), (9, 100), (4, 255), (16, 256), (3, 2048), (3, 2049),
-          (40, 4096), (2, 5000), (3, 16384), (2, 16385), (2, 65536), (2, 100003)]
+          (40, 4096), (2, 5000), (3, 16384), (2, 16385), (3, 32768),
+          # rows split across a cluster: parts in registers (2 to 16 CTAs) ...
+          (3, 32769), (3, 40000), (3, 65536), (3, 100003), (3, 262144), (3, 524288),
+          # ... and rows streamed twice by the cluster's CTAs
+          (3, 524296), (3, 1048576), (3, 1048573)]
 
 
 def make_rows(rows, N, dtype, seed, scale=3.0):
@@ -66,3 +70,24 @@ def test_softmax_rows_worked_example():
     torch.cuda.synchronize()
     np.testing.assert_allclose(y.cpu().numpy()[0], [0.0159, 0.8668, 0.1173], atol=1e-4)
     assert abs(l.item() - (5 + np.log(1.1536))) < 1e-4
+
+
+@pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
+@pytest.mark.parametrize("N", [65536, 262144, 1048576])
+def test_split_row_with_a_cluster_part_fully_masked(N, dtype):
+    # Whole parts of a split row masked (-inf): their CTAs hold the empty
+    # state (-inf, 0), which the guarded combine across the cluster must
+    # absorb without NaN; one row masked everywhere but its last element.
+    g = torch.Generator().manual_seed(N)
+    x = torch.randn(3, N, generator=g) * 3.0
+    x[0, N // 8: N // 2] = -float("inf")
+    x[1, : N - 1] = -float("inf")
+    x[2, N // 2:] = -float("inf")
+    x = x.to(dtype)
+    xd = x.to(DEV)
+    y, lse = osattn.softmax_rows(xd)
+    assert osattn.get_device_status() == osattn.OK
+    Yref, Lref = oracle.softmax_rows(x)
+    Y = y.double().cpu().numpy()
+    check(Y, lse.double().cpu().numpy(), Yref, Lref, KIND[dtype])
+    assert Y[1, -1] == 1.0 and np.all(Y[1, :-1] == 0.0)
