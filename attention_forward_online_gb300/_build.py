@@ -32,25 +32,35 @@ def _deps():
         os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# A profiling build of the same sources with the forward kernel's per-step
+# clock stamps compiled in (OSATTN_STEP_TRACE=1); never loaded by default.
+TRACE_LIB = os.path.join(PKG, "libosattn_trace.so")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          step_trace: bool = False) -> str:
+    lib = TRACE_LIB if step_trace else LIB
+    if not force and up_to_date(lib):
+        return lib
+    build_dir = BUILD_DIR + ("_trace" if step_trace else "")
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]
+    if step_trace:
+        common += ["-DOSATTN_STEP_TRACE=1"]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,13 +72,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -56,6 +56,29 @@
 #include "tc_attn_mma.cuh"
 
 namespace osattn {
+
+// Profiling builds (OSATTN_STEP_TRACE=1, a separate library; never the
+// product) stamp the SM clock at each phase of every K/V step of the first
+// kTraceCtas CTAs: per softmax warpgroup t (role t) S seen / S in registers /
+// alpha published / P published, and in the MMA thread (role 2) K/V seen /
+// P_0 seen / P_1 seen / step issued.  osattn_step_trace_read copies them out.
+#ifndef OSATTN_STEP_TRACE
+#define OSATTN_STEP_TRACE 0
+#endif
+constexpr int kTraceCtas = 8, kTraceSteps = 128;
+#if OSATTN_STEP_TRACE
+__device__ long long g_step_trace[kTraceCtas][3][kTraceSteps][4];
+#define OSATTN_STAMP(cond, role, j, k)                                                  \
+  do {                                                                                  \
+    if ((cond) && blockIdx.x < kTraceCtas && (j) < kTraceSteps)                         \
+      g_step_trace[blockIdx.x][role][j][k] = clock64();                                 \
+  } while (0)
+#else
+#define OSATTN_STAMP(cond, role, j, k) \
+  do {                                 \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int BM = 128;     // query rows per tile (MMA M, tensor-memory lanes)
@@ -207,6 +230,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     ok = mbar_wait(&bars->s_full[t], static_cast<uint32_t>(j) & 1u, wc, kSiteSoftS);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
+    OSATTN_STAMP(row == 0, t, j, 0);
     tc_fence_after_sync();
     uint32_t v[BN];
 #pragma unroll
@@ -214,6 +238,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     tmem_ld_wait();
 #pragma unroll
     for (int ch = 0; ch < BN / 32; ++ch) reg_fence32(v + ch * 32);
+    OSATTN_STAMP(row == 0, t, j, 1);
 
     // x_j = s_j * c (log2 units).  Unmasked tiles keep raw s in v and fold
     // the scale into the exponent's FMA (cm = c); tiles crossing key_len or
@@ -233,6 +258,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
     bars->alpha[t][row] = alpha;
     mbar_arrive(&bars->alpha_full[t]);
+    OSATTN_STAMP(row == 0, t, j, 2);
 
     // P = 2^(x - m_new) in pairs (f32x2 FMA, two MUFU ex2, f32x2 add for the
     // row sum), packed to bf16 and stored over S in two halves of 32
@@ -268,6 +294,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     tmem_st_wait();
     tc_fence_before_sync();
     mbar_arrive(&bars->p_full[t]);
+    OSATTN_STAMP(row == 0, t, j, 3);
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -478,6 +505,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
     const uint32_t ks = static_cast<uint32_t>((2 * j) % C::kStages);
     ok = mbar_wait(&bars->kv_full[j % C::kIters], static_cast<uint32_t>(j / C::kIters) & 1u, wc,
                    kSiteMmaKV);
+    OSATTN_STAMP(true, 2, j, 0);
     if (ok && j == 0) {
       if (n0 > 0) ok = mbar_wait(&bars->q_full[0], 0, wc, kSiteMmaQ);
       if (ok && n1 > 0) ok = mbar_wait(&bars->q_full[1], 0, wc, kSiteMmaQ);
@@ -487,6 +515,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
     // tile 0: PV0(j-1), then S0(j)
     if (j > 0 && j - 1 < n0) {
       ok = mbar_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      OSATTN_STAMP(true, 2, j, 1);
       if (!ok) break;
       tc_fence_after_sync();
       mma_tmem_a_128<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
@@ -499,6 +528,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
     // tile 1: PV1(j-1), then S1(j)
     if (j > 0 && j - 1 < n1) {
       ok = mbar_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      OSATTN_STAMP(true, 2, j, 2);
       if (!ok) break;
       tc_fence_after_sync();
       mma_tmem_a_128<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
@@ -509,6 +539,7 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
       mma_commit(&bars->s_full[1]);
     }
     mma_commit(&bars->kv_empty[j % C::kIters]);
+    OSATTN_STAMP(true, 2, j, 3);
   }
   // Every MMA this thread issued must complete before tensor memory is freed.
   mma_commit(&bars->mma_drain);
@@ -661,6 +692,18 @@ cudaError_t prepare_fwd_bf16() {
   if ((e = set_attrs<128, false, true>()) != cudaSuccess) return e;
   if ((e = set_attrs<64, true, true>()) != cudaSuccess) return e;
   return set_attrs<128, true, true>();
+}
+
+cudaError_t read_step_trace(void* host, size_t bytes, size_t* needed) {
+  *needed = static_cast<size_t>(kTraceCtas) * 3 * kTraceSteps * 4 * sizeof(long long);
+#if OSATTN_STEP_TRACE
+  if (bytes < *needed) return cudaErrorInvalidValue;
+  return cudaMemcpyFromSymbol(host, g_step_trace, *needed);
+#else
+  (void)host;
+  (void)bytes;
+  return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,

@@ -680,6 +680,15 @@ int osattn_softmax_rows(const void* in, void* out, float* lse, int64_t rows, int
   return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
 }
 
+int osattn_step_trace_read(void* host, size_t bytes, size_t* needed) {
+  size_t n = 0;
+  const cudaError_t e = osattn::read_step_trace(host, bytes, &n);
+  if (needed) *needed = n;
+  if (e == cudaErrorNotSupported) return OSATTN_ERR_UNSUPPORTED;
+  if (e == cudaErrorInvalidValue) return OSATTN_ERR_INVALID_ARG;
+  return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
+}
+
 int osattn_get_device_status(void* stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st);

@@ -41,6 +41,9 @@ cudaError_t launch_fwd_fp32(const FwdArgs& a);
 // maps describe Q, K and V as 4-D views (d, N, H, B) with the caller's
 // strides and 128-byte swizzled 64 x 128 boxes.
 cudaError_t prepare_fwd_bf16();  // once per device: kernel attributes
+// Copies the forward kernel's per-step clock stamps (profiling builds) to
+// host memory; *needed gets their size.  cudaErrorNotSupported otherwise.
+cudaError_t read_step_trace(void* host, size_t bytes, size_t* needed);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV);
 

@@ -36,7 +36,7 @@ EXPORTS = ("osattn_fwd", "osattn_fwd_strided", "osattn_fwd_splitkv",
            "osattn_softmax_rows_offload",
            "osattn_status_string", "osattn_get_device_status",
            "osattn_version", "osattn_set_wait_limit_ns", "osattn_test_wait_timeout",
-           "osattn_last_timeout_site")
+           "osattn_last_timeout_site", "osattn_step_trace_read")
 
 _lock = threading.Lock()
 _lib = None
@@ -107,8 +107,24 @@ def lib():
             L.osattn_test_wait_timeout.restype = i32
             L.osattn_last_timeout_site.argtypes = []
             L.osattn_last_timeout_site.restype = i32
+            L.osattn_step_trace_read.argtypes = [vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+            L.osattn_step_trace_read.restype = i32
             _lib = L
         return _lib
+
+
+def step_trace():
+    """The per-step clock stamps of a profiling build (OSATTN_STEP_TRACE=1;
+    see include/osattn.h) as a numpy int64 array [8, 3, 128, 4]."""
+    import numpy as np
+
+    need = ctypes.c_size_t(0)
+    lib().osattn_step_trace_read(None, 0, ctypes.byref(need))
+    buf = np.zeros(need.value // 8, dtype=np.int64)
+    st = lib().osattn_step_trace_read(buf.ctypes.data, buf.nbytes, ctypes.byref(need))
+    if st != OK:
+        raise OsattnError(st, "osattn_step_trace_read")
+    return buf.reshape(8, 3, 128, 4)
 
 
 def status_string(status: int) -> str:

@@ -1,7 +1,7 @@
 """Run libosattn on one workload a fixed number of times (for profilers).
 
     python -m attention_forward_online_gb300.run_workload --workload NAME
-        [--launches N] [--heads H]
+        [--launches N] [--heads H] [--step-trace]
 
 Inputs are the seeded synthetic tensors of the named workload, resident on
 cuda:0 before the first launch; --heads keeps only the first H heads (a
@@ -10,6 +10,11 @@ backward workload runs the forward pass once, untimed, and then times the
 backward call (its three kernels).  A row-softmax workload runs
 osattn_softmax_rows (--heads then keeps that many thousand rows).  Prints
 the median launch time from CUDA events on the launching stream.
+
+--step-trace builds and loads the profiling library (the forward kernel's
+per-step SM clock stamps compiled in, libosattn_trace.so) and prints, for
+the first CTAs of the last launch, the steady-state cycles per K/V step and
+how each role spends them.
 """
 import argparse
 import dataclasses
@@ -34,9 +39,15 @@ def main(argv=None):
     ap.add_argument("--workload", required=True, choices=sorted(allw))
     ap.add_argument("--launches", type=int, default=4)
     ap.add_argument("--heads", type=int, default=0)
+    ap.add_argument("--step-trace", action="store_true",
+                    help="profile the forward kernel's K/V steps (profiling build)")
     ap.add_argument("--splits", type=int, default=-1,
                     help="key ranges for the split-KV entry point (0: unsplit; default: the workload's)")
     args = ap.parse_args(argv)
+    if args.step_trace:
+        from attention_forward_online_gb300 import _build
+
+        osattn.LIB_PATH = _build.build(step_trace=True)
     w = allw[args.workload]
     if args.workload in ROW_WORKLOADS:
         return run_rows(w, args)
@@ -85,7 +96,34 @@ def main(argv=None):
     print(f"{w.name} H={w.H} splits={w.splits}: launches {args.launches}, median {med:.4f} ms = "
           f"{flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
           f"ms {['%.4f' % m for m in ms]}")
+    if args.step_trace:
+        print_step_trace(osattn.step_trace())
     return 0
+
+
+def print_step_trace(tr):
+    """Steady-state summary of the forward kernel's per-step clock stamps
+    (tr [cta, role, step, stamp], see osattn_step_trace_read): the steps
+    after the first two and before the last of each traced CTA."""
+    import numpy as np
+
+    for cta in range(tr.shape[0]):
+        sm0, sm1, mma = tr[cta, 0], tr[cta, 1], tr[cta, 2]
+        n = int((sm0[:, 3] > 0).sum())
+        if n < 6:
+            continue
+        js = np.arange(2, n - 1)
+        step = np.diff(sm0[js, 0]).mean()
+        ld = (sm0[js, 1] - sm0[js, 0]).mean()
+        mx = (sm0[js, 2] - sm0[js, 1]).mean()
+        pp = (sm0[js, 3] - sm0[js, 2]).mean()
+        # from P published (step j) to S of step j+1 seen: the tile's MMAs
+        mma_lat = (sm0[js[:-1] + 1, 0] - sm0[js[:-1], 3]).mean()
+        mma_iter = np.diff(mma[js, 0]).mean()
+        print(f"CTA {cta}: {n} steps; cycles per K/V step {step:.0f}; softmax of tile 0: "
+              f"S load {ld:.0f}, row max + alpha {mx:.0f}, P {pp:.0f} "
+              f"(busy {ld + mx + pp:.0f}); P published -> next S seen (PV + S) {mma_lat:.0f}; "
+              f"MMA issuer iteration {mma_iter:.0f}")
 
 
 def run_rows(w, args):

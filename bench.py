@@ -19,6 +19,11 @@ osattn_fwd_offload (the library's host-memory entry point, which pipelines
 the copies with the compute over chunks of heads); split-KV workloads copy,
 call and copy back in sequence.
 
+other_configs: with the default workload, the other two large forward
+workloads (causal B=4 H=16 N=4096 d=64 and B=8 H=40 N=2048 d=128) are timed
+the same way, kernel only, each with its own clock record and the max-abs
+error of 256 sampled rows against the oracle.
+
 cpu_baseline: the fp64 oracle as it stands, timed on this host's cores on a
 bounded random sample of query rows of the same workload (about 10-20 s of
 CPU work) and scaled to TFLOPS by the sample's own FLOPs; the GPU's outputs
@@ -321,6 +326,61 @@ def run_reference(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ other configs
+# The other two large forward workloads, timed kernel-only beside the
+# headline one (the line's `other_configs`).
+OTHER_CONFIGS = ("bf16_causal_b4_h16_n4096_d64", "bf16_b8_h40_n2048_d128")
+
+
+def measure_other_configs(torch, dev, stream, flush, args, world, local, rank, peak):
+    """Kernel-only CUDA-event timing of each OTHER_CONFIGS workload (3
+    warm-up calls, then min(steps, 20) timed calls with the L2 flushed
+    between them and the clocks sampled), and on rank 0 the max-abs error
+    of 256 sampled rows against the oracle."""
+    import numpy as np
+
+    from attention_forward_online_gb300 import osattn
+    from attention_forward_online_gb300.inputs import WORKLOADS, make_inputs, sample_rows
+
+    out = []
+    for name in OTHER_CONFIGS:
+        w = WORKLOADS[name]
+        q, k, v, _ = make_inputs(w)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        O = torch.empty_like(qd)
+        L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+
+        def step():
+            osattn.fwd(qd, kd, vd, scale=w.scale, causal=w.causal, out=O, lse=L, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        stream.synchronize()
+        steps = max(3, min(args.steps, 20))
+        ms, clocks = timed_steps(torch, dev, stream, step, flush, steps, world, local)
+        if osattn.get_device_status(stream) != osattn.OK:
+            raise RuntimeError(f"device-side wait timed out on {name}")
+        avg = reduce_max(sum(ms), world) / steps
+        tflops = w.flops / (avg * 1e-3) / 1e12
+        rec = {"workload": name, "steps": steps, "ms_per_launch": round(avg, 4),
+               "tflops": round(tflops, 2), "pct_of_bf16_peak": round(100 * tflops / peak, 2),
+               "clocks": clocks}
+        if rank == 0:
+            import oracle
+
+            rows = sample_rows(w.B, w.H, w.Nq, 256, seed=11)
+            Oref, Lref = oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=rows)
+            idx = torch.tensor(rows, device=dev)
+            Og = O.reshape(-1, w.d)[idx].double().cpu().numpy()
+            Lg = L.reshape(-1)[idx].double().cpu().numpy()
+            rec["max_abs_err"] = {"O": float(np.abs(Og - Oref).max()),
+                                  "LSE": float(np.abs(Lg - Lref).max()), "rows_checked": len(rows)}
+        out.append(rec)
+        del qd, kd, vd, O, L
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, w):
     import torch
@@ -402,6 +462,10 @@ def run_ours(args, w):
     e2e_value = world * w.flops / (e2e_ms * 1e-3) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = Oh.numel() * Oh.element_size() + Lh.numel() * Lh.element_size()
+    others = []
+    if args.other_configs:
+        others = measure_other_configs(torch, dev, stream, flush, args, world, local, rank,
+                                       float(peaks["bf16_tflops"]))
 
     line = None
     if rank == 0:
@@ -449,6 +513,8 @@ def run_ours(args, w):
             "clocks": clock_info,
             "kernel_source_sha": kernel_source_hash(),
         }
+        if others:
+            line["other_configs"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -703,7 +769,13 @@ def main(argv=None):
     ap.add_argument("--workload", default=BENCH_WORKLOAD,
                     choices=sorted(allw) + sorted(ROW_WORKLOADS) + sorted(BWD_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--other-configs", dest="other_configs", action="store_true", default=None,
+                    help="also time the other large forward workloads (default: with the "
+                         "default workload only)")
+    ap.add_argument("--no-other-configs", dest="other_configs", action="store_false")
     args = ap.parse_args(argv)
+    if args.other_configs is None:
+        args.other_configs = args.workload == BENCH_WORKLOAD
     if args.workload in ROW_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

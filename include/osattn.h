@@ -421,6 +421,21 @@ int osattn_test_wait_timeout(void* stream);
  * Codes identify the waiting role (producer, MMA issuer, softmax, epilogue). */
 int osattn_last_timeout_site(void);
 
+/*
+ * osattn_step_trace_read - profiling hook (no counterpart in the method).
+ * A library built with OSATTN_STEP_TRACE=1 (a separate profiling build,
+ * never the product) records SM clock stamps at the phases of every K/V
+ * step of the first 8 CTAs of each bf16/fp16 forward launch: long long
+ * [8 CTAs][3 roles][128 steps][4 stamps]; role 0/1 = softmax of query tile
+ * 0/1 (S seen, S in registers, alpha published, P published), role 2 = MMA
+ * issuer (K/V seen, P of tile 0 seen, P of tile 1 seen, step issued).
+ * Copies them to `host` (bytes >= *needed) after the stream has
+ * synchronised.  *needed (if not NULL) gets the size.  Returns OSATTN_OK,
+ * OSATTN_ERR_INVALID_ARG (buffer too small) or, in a product build,
+ * OSATTN_ERR_UNSUPPORTED.
+ */
+int osattn_step_trace_read(void* host, size_t bytes, size_t* needed);
+
 #ifdef __cplusplus
 }
 #endif
