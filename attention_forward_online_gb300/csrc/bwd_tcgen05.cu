@@ -11,18 +11,20 @@
 //   dP_ij = <dO_i, V_j>,  dS_ij = P_ij (dP_ij - D_i)
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j.
 //
-// Three launches on one stream:
-//   bwd_rowdot_kernel  D = rowsum(dO * O) in fp32 (HBM-bound, 16-byte loads).
+// Two launches on one stream:
+//   bwd_dq_kernel      one CTA per 128-row query tile: Q and dO stay, the
+//                      visible K/V tiles stream.  Per key tile:
+//                        S = Q K^T  and  dP = dO V^T;  dS in 16-bit over dP
+//                        dQ += dS K                            (A from tensor memory)
+//                      It also forms D = rowsum(dO * O) of its rows (dO from
+//                      its resident tile, O read once) and writes it for:
 //   bwd_dkdv_kernel    one CTA per 128-key tile of a (b, h): K and V stay in
 //                      shared memory while the query tiles that can see
 //                      those keys stream through a TMA ring.  Per query tile:
 //                        S^T  = K Q^T   and  dP^T = V dO^T   (tensor memory)
 //                        P^T, dS^T in 16-bit over the first 64 columns of each
 //                        dV += P^T dO   and  dK += dS^T Q     (A from tensor memory)
-//   bwd_dq_kernel      one CTA per 128-row query tile: Q and dO stay, the
-//                      visible K/V tiles stream.  Per key tile:
-//                        S = Q K^T  and  dP = dO V^T;  dS in 16-bit over dP
-//                        dQ += dS K                            (A from tensor memory)
+// (bwd_rowdot_kernel forms D on its own for the fp32 path.)
 // S and dP are computed twice (once per kernel) so that no kernel needs
 // atomics: each output element is written once, by one CTA.
 //
@@ -89,8 +91,10 @@ struct __align__(16) BwdBars {
   uint64_t ds_full;               // elementwise -> MMA: dS or dS^T written (256 arrivals)
   uint64_t acc_full;              // MMA -> epilogue: the last accumulation is done
   uint64_t mma_drain;
+  uint64_t d_full;                // dQ kernel: both warpgroups' halves of D stored (256)
   uint32_t tmem_base;
   int abort_flag;
+  float d_part[2][kT];            // dQ kernel: D of each row over each warpgroup's columns
 };
 
 template <int HD>
@@ -111,7 +115,9 @@ struct BwdParams {
   uint16_t* dV;
   long long dq_s[3], dk_s[3], dv_s[3];  // element strides of the b, h and row axes
   const float* LSE;
-  const float* D;
+  float* D;              // [B*H*Nq]: written by the dQ kernel, read by the dK/dV kernel
+  const uint16_t* O;     // forward output (for D), with its b, h, row element strides
+  long long o_s[3];
   const int32_t* key_len;
   int H, Nq, Nkv;
   int num_tiles;     // 128-row tiles per (b, h): of keys (dK/dV) or queries (dQ)
@@ -695,6 +701,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_drain, 1);
+    mbar_init(&bars->d_full, 256);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -796,13 +803,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int q = q0 + row;
     const bool row_live = q < p.Nq;
     const long long rix = static_cast<long long>(bh) * p.Nq + q;
-    float l2 = -INFINITY, Dq = 0.f;  // negated: -LSE * log2(e) and -D
+    float l2 = -INFINITY;  // negated: -LSE * log2(e)
+    // D = rowsum(dO * O) of this row: warpgroup g takes columns
+    // g * d/2 .. (g + 1) * d/2 - 1, O from global memory (loaded now, used
+    // after the first P part), dO from the resident tile.
+    using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
+    constexpr int kHalfD = HD / 2, kNv = kHalfD / 8;  // 16-byte vectors of the half row
+    const int g = warp >> 2;
+    uint4 ov[kNv];
+#pragma unroll
+    for (int v = 0; v < kNv; ++v) ov[v] = make_uint4(0u, 0u, 0u, 0u);
     if (row_live && n_kt > 0) {
       const float L = p.LSE[rix];
       l2 = (L == -INFINITY) ? -INFINITY : -(L * kLog2e);
-      Dq = -p.D[rix];
+      const uint4* orow = reinterpret_cast<const uint4*>(
+          p.O + b * p.o_s[0] + h * p.o_s[1] + static_cast<long long>(q) * p.o_s[2] + g * kHalfD);
+#pragma unroll
+      for (int v = 0; v < kNv; ++v) ov[v] = orow[v];
     }
-    const float4 l2v = make_float4(l2, l2, l2, l2), dv4 = make_float4(Dq, Dq, Dq, Dq);
+    const float4 l2v = make_float4(l2, l2, l2, l2);
+    float4 dv4 = make_float4(0.f, 0.f, 0.f, 0.f);  // -D
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     bool ok = true;
     for (int j = 0; ok && j < n_kt; ++j) {
@@ -822,6 +842,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_p_part<kF16, false, false>(lane_base + 128 * (j & 1), c0, p.scale_log2, vis, l2of4, pr);
       else
         bwd_p_part<kF16, false, true>(lane_base + 128 * (j & 1), c0, p.scale_log2, vis, l2of4, pr);
+      if (j == 0) {
+        // the half dot product of D over this warpgroup's columns of the
+        // swizzled dO tile (16-byte chunk c of a 128-byte row sits at
+        // chunk c ^ (row mod 8)), then both halves through shared memory
+        ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdElem);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        float part = 0.f;
+#pragma unroll
+        for (int v = 0; v < kNv; ++v) {
+          const int col = g * kHalfD + v * 8;  // first of the vector's 8 columns
+          const uint4 gv = *reinterpret_cast<const uint4*>(
+              sdO + (col / 64) * kT * 128 + row * 128 + ((((col % 64) / 8) ^ (row & 7)) * 16));
+          const uint32_t ow[4] = {ov[v].x, ov[v].y, ov[v].z, ov[v].w};
+          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = unpack2<T>(ow[e]), y = unpack2<T>(gw[e]);
+            part = fmaf(x.x, y.x, fmaf(x.y, y.y, part));
+          }
+        }
+        bars->d_part[g][row] = part;
+        mbar_arrive(&bars->d_full);
+        ok = mbar_wait(&bars->d_full, 0, wc, kSiteBwdElem);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const float D = bars->d_part[0][row] + bars->d_part[1][row];
+        dv4 = make_float4(-D, -D, -D, -D);
+        if (g == 0 && row_live) p.D[rix] = D;
+      }
       ok = mbar_wait(&bars->dp_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdElem);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -889,9 +939,6 @@ cudaError_t launch_rowdot(const BwdArgs& a) {
 template <int HD, bool kF16>
 cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensorMap& tmQ,
                          const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmdO) {
-  using T = typename std::conditional<kF16, __half, __nv_bfloat16>::type;
-  cudaError_t e = launch_rowdot<T>(a);
-  if (e != cudaSuccess) return e;
   // Causal CTA groups: heads whose streamed tiles (Q and dO for dK/dV, K
   // and V for dQ) take about 32 MB of L2 together.
   auto group = [&](int rows) {
@@ -911,12 +958,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, const BwdParams& base, const CUtensor
   pq.num_tiles = (a.Nq + kT - 1) / kT;
   const long long gq = static_cast<long long>(pq.num_tiles) * a.B * a.H;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
-  bwd_dkdv_kernel<HD, kF16><<<static_cast<unsigned>(gk), kBwdThreads, dkdv_smem_bytes<HD>(), a.stream>>>(
-      tmQ, tmK, tmV, tmdO, pk);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // dQ first: it also writes D, which the dK/dV kernel reads
   bwd_dq_kernel<HD, kF16><<<static_cast<unsigned>(gq), kBwdThreads, dq_smem_bytes<HD>(), a.stream>>>(
       tmQ, tmK, tmV, tmdO, pq);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<HD, kF16><<<static_cast<unsigned>(gk), kBwdThreads, dkdv_smem_bytes<HD>(), a.stream>>>(
+      tmQ, tmK, tmV, tmdO, pk);
   return cudaGetLastError();
 }
 
@@ -945,6 +993,8 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tmQ, const CUtensorM
   }
   p.LSE = a.LSE;
   p.D = a.D;
+  p.O = static_cast<const uint16_t*>(a.O);
+  for (int i = 0; i < 3; ++i) p.o_s[i] = a.o_strides[i];
   p.key_len = a.key_len;
   p.H = a.H;
   p.Nq = a.Nq;
