@@ -365,7 +365,7 @@ def measure_other_configs(torch, dev, stream, flush, args, world, local, rank, p
         tflops = w.flops / (avg * 1e-3) / 1e12
         rec = {"workload": name, "steps": steps, "ms_per_launch": round(avg, 4),
                "tflops": round(tflops, 2), "pct_of_bf16_peak": round(100 * tflops / peak, 2),
-               "clocks": clocks}
+               "traffic": committed_traffic(name), "clocks": clocks}
         if rank == 0:
             import oracle
 
