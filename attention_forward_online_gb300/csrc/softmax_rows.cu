@@ -31,11 +31,13 @@
 #include <cuda_fp16.h>
 
 #include "osattn_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace osattn {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // The combine of two (m, l) states, branch-free: when both are empty the
 // exponent base is taken as 0 instead of -inf, so e^{-inf - 0} = 0 keeps
@@ -66,13 +68,6 @@ __device__ __forceinline__ void block_combine(float& m, float& l, float* sm, int
   for (int off = 16; off > 0; off >>= 1)
     combine(m, l, __shfl_xor_sync(kFull, m, off), __shfl_xor_sync(kFull, l, off));
   __syncthreads();  // sm is reused for the next row
-}
-
-// Three-input max (one instruction on sm_100 and later).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
 }
 
 // ---- thread-block cluster primitives (PTX)
@@ -244,27 +239,39 @@ __global__ void __launch_bounds__(1024) softmax_rows_regs(const T* __restrict__ 
           v[i * EPV + e] = base + e < N ? Vec<T>::get(x, base + e) : -INFINITY;
       }
     }
-    // this thread's block: max, then the exponentials and their sum
+    // this thread's block: max, then the exponentials and their sum.  The
+    // arithmetic runs on pairs (f32x2: one instruction for two elements,
+    // the same rounding as scalar code): 16-bit rows are bound by issue.
     float m = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < E; ++e) m = fmaxf(m, v[e]);
+    for (int e = 0; e < E; e += 2) m = fmax3(m, v[e], v[e + 1]);
     const float base_t = m == -INFINITY ? 0.f : m;  // all-masked thread: every e^{-inf} = 0
-    float l = 0.f;
+    // e^{x - base} = 2^{x log2(e) - base log2(e)}: one fused multiply-add a pair
+    const uint64_t k2 = f2_pack(kLog2e, kLog2e), nb2 = f2_pack(-base_t * kLog2e, -base_t * kLog2e);
+    uint64_t l2 = 0;  // bit pattern 0 = (0.0f, 0.0f)
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      v[e] = __expf(v[e] - base_t);
-      l += v[e];
+    for (int e = 0; e < E; e += 2) {
+      float a, b;
+      f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), k2, nb2), a, b);
+      v[e] = ex2_approx(a);
+      v[e + 1] = ex2_approx(b);
+      l2 = f2_add(l2, f2_pack(v[e], v[e + 1]));
     }
+    float la, lb;
+    f2_unpack(l2, la, lb);
+    float l = la + lb;
     const float m_t = m;
     block_combine(m, l, sm, warps);
     // y = e^{x - m_t} * e^{m_t - M} / L  (0 for a row with no finite entry)
     const float f = l > 0.f ? __expf(m_t - m) / l : 0.f;
+    const uint64_t f2 = f2_pack(f, f);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int base = (i * nt + threadIdx.x) * EPV;
       float o[EPV];
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) o[e] = v[i * EPV + e] * f;
+      for (int e = 0; e < EPV; e += 2)
+        f2_unpack(f2_mul(f2_pack(v[i * EPV + e], v[i * EPV + e + 1]), f2), o[e], o[e + 1]);
       if (kVec) {
         if (base < N) Vec<T>::store(y + base, o);
       } else {
