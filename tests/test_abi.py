@@ -345,3 +345,13 @@ def test_bwd_offload_host_validation(L, kw, expect):
 ])
 def test_softmax_rows_offload_host_validation(L, args, expect):
     assert L.osattn_softmax_rows_offload(*args, ctypes.c_void_p(None)) == expect
+
+
+def test_step_trace_hook_is_unsupported_in_the_product_build(L):
+    # The per-step clock stamps exist only in the separate profiling build
+    # (OSATTN_STEP_TRACE=1); the product library answers UNSUPPORTED without
+    # touching the device, and still reports the buffer size a trace needs.
+    need = ctypes.c_size_t(0)
+    rc = L.osattn_step_trace_read(None, 0, ctypes.byref(need))
+    assert rc == osattn.ERR_UNSUPPORTED
+    assert need.value == 8 * 3 * 128 * 4 * 8
