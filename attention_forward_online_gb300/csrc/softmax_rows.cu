@@ -14,10 +14,10 @@
 // reduces its part of the row to one (m, l) state, the states meet through
 // distributed shared memory and every CTA merges them with the same guarded
 // combine.  Up to (cluster size) x 32768 elements the parts stay in the
-// CTAs' registers as fp32, and 16-bit rows up to (cluster size) x 65536 in
-// their packed form (one read, one write per element); beyond that each CTA
+// CTAs' registers (one read, one write per element); beyond that each CTA
 // streams its part twice (the three accesses of §6.7.4), the second read
-// served mostly by L2 because a cluster's part of the row was just read.
+// served mostly by L2 because a cluster's part of the row was just read,
+// with two CTAs per SM so that one part's reads overlap another's writes.
 //
 // Inside one thread the elements are a block: its max first, then
 // sum e^{x - m_t}, which is the blocked form of the recurrence (§6.6); the
@@ -26,7 +26,6 @@
 // (-inf, 0) state; its output is 0 and its LSE -inf (never NaN).
 #include <cmath>
 #include <cstdint>
-#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -170,11 +169,6 @@ struct Vec<__nv_bfloat16> {
   }
   __device__ static float get(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
   __device__ static void put(__nv_bfloat16* p, long long i, float v) { p[i] = __float2bfloat16_rn(v); }
-  // the two elements of a packed word, as floats; an element's 16 bits
-  __device__ static float2 word(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-  }
-  __device__ static uint32_t bits(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
 };
 template <>
 struct Vec<__half> {
@@ -200,11 +194,6 @@ struct Vec<__half> {
   }
   __device__ static float get(const __half* p, long long i) { return __half2float(p[i]); }
   __device__ static void put(__half* p, long long i, float v) { p[i] = __float2half_rn(v); }
-  // the two elements of a packed word, as floats; an element's 16 bits
-  __device__ static float2 word(uint32_t w) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&w));
-  }
-  __device__ static uint32_t bits(__half v) { return __half_as_ushort(v); }
 };
 
 // Row held in registers: each thread owns NV 16-byte vectors (32 elements),
@@ -358,99 +347,6 @@ __global__ void __launch_bounds__(1024) softmax_rows_cluster_regs(const T* __res
   }
 }
 
-// 16-bit rows up to (cluster size) x 65536 elements: as the kernel above
-// but each thread keeps its 64 elements in their packed 16-bit form (eight
-// 16-byte vectors, 32 registers), so the cluster holds twice as many; the
-// exponentials are taken twice (for the sum, then for the output) instead
-// of being kept.  One read and one write per element.
-template <typename T, bool kVec>
-__global__ void __launch_bounds__(1024) softmax_rows_cluster_packed(const T* __restrict__ in,
-                                                                    T* __restrict__ out,
-                                                                    float* __restrict__ lse,
-                                                                    long long rows, int N) {
-  constexpr int EPV = Vec<T>::N;  // 8
-  constexpr int NV = 8;           // vectors per thread
-  __shared__ float sm[68];
-  const int nt = blockDim.x, warps = nt >> 5;
-  const int C = static_cast<int>(cluster_size());
-  const uint32_t rank = cluster_rank();
-  const long long c0 = static_cast<long long>(rank) * nt * NV * EPV;
-  const int n_here =
-      static_cast<int>(max(0LL, min(static_cast<long long>(nt) * NV * EPV, N - c0)));
-  for (long long row = cluster_id(); row < rows; row += cluster_count()) {
-    const T* x = in + row * N + c0;
-    T* y = out + row * N + c0;
-    uint4 w[NV];
-    // -inf in both halves of a word: 0xff80 (bf16) or 0xfc00 (fp16)
-    constexpr uint32_t kNegInf2 = sizeof(T) == 2 && std::is_same<T, __half>::value ? 0xfc00fc00u
-                                                                                    : 0xff80ff80u;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int base = (i * nt + threadIdx.x) * EPV;
-      if (kVec) {
-        w[i] = base < n_here ? *reinterpret_cast<const uint4*>(x + base)
-                             : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
-      } else {
-        uint32_t ws[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t lo = base + 2 * k < n_here ? Vec<T>::bits(x[base + 2 * k]) : kNegInf2 & 0xffffu;
-          const uint32_t hi =
-              base + 2 * k + 1 < n_here ? Vec<T>::bits(x[base + 2 * k + 1]) : kNegInf2 & 0xffffu;
-          ws[k] = lo | (hi << 16);
-        }
-        w[i] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-      }
-    }
-    // word by word (two elements), so that few values are live beside w
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = Vec<T>::word(ws[k]);
-        m = fmax3(m, f.x, f.y);
-      }
-    }
-    const float base_t = m == -INFINITY ? 0.f : m;
-    float l = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = Vec<T>::word(ws[k]);
-        l += __expf(f.x - base_t) + __expf(f.y - base_t);
-      }
-    }
-    block_combine(m, l, sm, warps);
-    cluster_combine(m, l, sm, C);
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
-    const float mb = m == -INFINITY ? 0.f : m;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int base = (i * nt + threadIdx.x) * EPV;
-      const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-      float v[EPV];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = Vec<T>::word(ws[k]);
-        v[2 * k] = __expf(f.x - mb) * inv_l;
-        v[2 * k + 1] = __expf(f.y - mb) * inv_l;
-      }
-      if (kVec) {
-        if (base < n_here) Vec<T>::store(y + base, v);
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-          if (base + e < n_here) Vec<T>::put(y, base + e, v[e]);
-      }
-    }
-    if (lse && rank == 0 && threadIdx.x == 0) lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
-  }
-}
-
 // Rows beyond the cluster's registers: CTA `rank` owns elements
 // [rank * chunk, rank * chunk + chunk) and streams them twice - pass 1 for
 // its (m, l), folded per run of kU vectors (each run's max, then the sum of
@@ -494,17 +390,26 @@ __global__ void __launch_bounds__(1024) softmax_rows_cluster_stream(const T* __r
       }
       float rm = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < R; ++e) rm = fmaxf(rm, r[e]);
+      for (int e = 0; e < R; e += 2) rm = fmax3(rm, r[e], r[e + 1]);
       if (rm == -INFINITY) continue;  // an all-masked run leaves the state alone
-      float rl = 0.f;
+      const uint64_t k2 = f2_pack(kLog2e, kLog2e), nb2 = f2_pack(-rm * kLog2e, -rm * kLog2e);
+      uint64_t rl2 = 0;
 #pragma unroll
-      for (int e = 0; e < R; ++e) rl += __expf(r[e] - rm);
-      combine(m, l, rm, rl);
+      for (int e = 0; e < R; e += 2) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(r[e], r[e + 1]), k2, nb2), a, b);
+        rl2 = f2_add(rl2, f2_pack(ex2_approx(a), ex2_approx(b)));
+      }
+      float ra, rb;
+      f2_unpack(rl2, ra, rb);
+      combine(m, l, rm, ra + rb);
     }
     block_combine(m, l, sm, warps);
     cluster_combine(m, l, sm, C);
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     const float mb = m == -INFINITY ? 0.f : m;
+    const uint64_t k2 = f2_pack(kLog2e, kLog2e), nb2 = f2_pack(-mb * kLog2e, -mb * kLog2e),
+                   inv2 = f2_pack(inv_l, inv_l);
     for (int k0 = 0; k0 < n_here; k0 += step) {
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
@@ -514,7 +419,11 @@ __global__ void __launch_bounds__(1024) softmax_rows_cluster_stream(const T* __r
           if (base < n_here) {
             Vec<T>::load(x + base, o);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) o[e] = __expf(o[e] - mb) * inv_l;
+            for (int e = 0; e < EPV; e += 2) {
+              float a, b;
+              f2_unpack(f2_fma(f2_pack(o[e], o[e + 1]), k2, nb2), a, b);
+              f2_unpack(f2_mul(f2_pack(ex2_approx(a), ex2_approx(b)), inv2), o[e], o[e + 1]);
+            }
             Vec<T>::store(y + base, o);
           }
         } else {
@@ -590,37 +499,21 @@ cudaError_t launch_any(const void* in, void* out, float* lse, long long rows, in
                : launch_cluster(softmax_rows_cluster_regs<T, NV, false>, C, threads, rows, num_sms,
                                 s, x, y, lse, rows, N);
   }
-  if constexpr (sizeof(T) == 2) {
-    constexpr int kPackedElems = 1024 * 64;  // elements one CTA holds packed
-    if (N <= static_cast<long long>(max_cluster) * kPackedElems) {
-      const int C = (N + kPackedElems - 1) / kPackedElems;
-      const int per = (N + C - 1) / C;
-      const int threads = ((per + 32 * 64 - 1) / (32 * 64)) * 32;
-      return vec ? launch_cluster(softmax_rows_cluster_packed<T, true>, C, threads, rows,
-                                  num_sms, s, x, y, lse, rows, N)
-                 : launch_cluster(softmax_rows_cluster_packed<T, false>, C, threads, rows,
-                                  num_sms, s, x, y, lse, rows, N);
-    }
-  }
   const int C = max_cluster;
   const int chunk = ((N + C - 1) / C + 7) / 8 * 8;  // a whole number of 16-byte vectors
-  return vec ? launch_cluster(softmax_rows_cluster_stream<T, true>, C, 1024, rows, num_sms, s, x,
-                              y, lse, rows, N, chunk)
-             : launch_cluster(softmax_rows_cluster_stream<T, false>, C, 1024, rows, num_sms, s, x,
-                              y, lse, rows, N, chunk);
+  // 512 threads a CTA: two CTAs (two rows' parts) per SM, so one part's
+  // reads overlap the other's writes and cluster barriers
+  return vec ? launch_cluster(softmax_rows_cluster_stream<T, true>, C, 512, rows, 2 * num_sms, s,
+                              x, y, lse, rows, N, chunk)
+             : launch_cluster(softmax_rows_cluster_stream<T, false>, C, 512, rows, 2 * num_sms, s,
+                              x, y, lse, rows, N, chunk);
 }
 
 template <typename T>
 cudaError_t allow_large_clusters() {
   constexpr int NV = 32 / Vec<T>::N;
   cudaError_t e;
-  if constexpr (sizeof(T) == 2) {
-    if ((e = cudaFuncSetAttribute(softmax_rows_cluster_packed<T, true>,
-                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(softmax_rows_cluster_packed<T, false>,
-                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-      return e;
-  }
+
   if ((e = cudaFuncSetAttribute(softmax_rows_cluster_regs<T, NV, true>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(softmax_rows_cluster_regs<T, NV, false>,
