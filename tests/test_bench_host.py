@@ -121,3 +121,29 @@ def test_timed_steps_remeasures_once_after_a_throttled_run(monkeypatch):
     ms, info, loops, calls = _run_timed(monkeypatch, [bad, dict(bad)])
     assert loops == 2 and info["reasons"] == ["hw_thermal_slowdown"]
     assert info["remeasured_after"] == "hw_thermal_slowdown"
+
+
+def test_other_configs_are_the_other_large_forward_workloads():
+    # The bench line's other_configs: the two large forward workloads besides
+    # the default one, each with a committed DRAM traffic record for the
+    # kernel source as it is now.
+    from attention_forward_online_gb300.inputs import BENCH_WORKLOAD, WORKLOADS
+
+    assert len(bench.OTHER_CONFIGS) == 2 and BENCH_WORKLOAD not in bench.OTHER_CONFIGS
+    big = sorted((w.flops, n) for n, w in WORKLOADS.items() if w.dtype == "bf16")[-3:]
+    assert {n for _, n in big} == set(bench.OTHER_CONFIGS) | {BENCH_WORKLOAD}
+    for name in (BENCH_WORKLOAD,) + tuple(bench.OTHER_CONFIGS):
+        assert bench.committed_traffic(name) is not None, name
+
+
+def test_other_configs_default_only_with_the_default_workload(monkeypatch):
+    seen = {}
+    monkeypatch.setattr(bench, "run_ours", lambda args, w: seen.setdefault("args", args) and 0)
+    bench.main(["--steps", "3"])
+    assert seen["args"].other_configs is True
+    seen.clear()
+    bench.main(["--steps", "3", "--workload", "bf16_b8_h40_n2048_d128"])
+    assert seen["args"].other_configs is False
+    seen.clear()
+    bench.main(["--steps", "3", "--no-other-configs"])
+    assert seen["args"].other_configs is False
