@@ -34,10 +34,11 @@
 //               commit per iteration frees both stages: the MMA thread
 //               (whose issue of one MMA takes most of the MMA's 64 cycles)
 //               spends as little as possible on barrier checks.
-//   warp 13     allocates tensor memory; one thread issues the MMAs in the
-//               order S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... so the
-//               tensor core computes one tile's S while the other tile's
-//               softmax runs (ping-pong between the two query tiles).
+//   warp 13     allocates tensor memory and issues the MMAs (warp-wide
+//               loop, one elected lane issuing) in the order S0_0, S1_0,
+//               PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... so the tensor core
+//               computes one tile's S while the other tile's softmax runs
+//               (ping-pong between the two query tiles).
 // Tensor memory (512 columns): S0 at 0, S1 at 128 (fp32, 128 x 128 each; P_t
 // overwrites the first 64 columns of S_t as packed bf16 pairs), O0 at 256,
 // O1 at 256 + d (fp32, 128 x d).
@@ -484,11 +485,23 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 // S_t = Q_t K^T (128 x 128 fp32 into tensor-memory columns [t*128, t*128+128))
 // is mma_abt_128; O_t (+)= P_t V, with P from tensor memory (bf16 pairs over
 // S_t) and V read MN-major from shared memory, is mma_tmem_a_128.
+//
+// The whole MMA warp runs this loop: every wait is warp-wide and each MMA
+// and commit is issued by the one lane elect.sync picks, so the loop's
+// control flow stays warp-uniform (a lane-0-only issuer let the tensor pipe
+// idle for about 150 cycles at each barrier wait).
+
+// A bounded wait whose result is the same in every lane of the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
+                                          uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, site));
+}
 
 template <int HD, bool kF16>
 __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ, uint8_t* sKV,
                                          int n0, int n1, WaitCtl wc) {
   using C = Cfg<HD>;
+  [[maybe_unused]] const bool lead = (threadIdx.x & 31) == 0;  // stamps only
   const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
   const uint64_t q_desc1 = q_desc0 + static_cast<uint64_t>(C::kQBytes >> 4);
   const uint64_t k_desc = sdesc_sw128(smem_u32(sKV), 16, 1024);       // stage 0, K-major
@@ -503,47 +516,48 @@ __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ,
     // K_j sits at load slot 2j, V_{j-1} at 2j - 1; one barrier covers both.
     const uint32_t vs = j > 0 ? static_cast<uint32_t>((2 * j - 1) % C::kStages) : 0u;
     const uint32_t ks = static_cast<uint32_t>((2 * j) % C::kStages);
-    ok = mbar_wait(&bars->kv_full[j % C::kIters], static_cast<uint32_t>(j / C::kIters) & 1u, wc,
+    ok = warp_wait(&bars->kv_full[j % C::kIters], static_cast<uint32_t>(j / C::kIters) & 1u, wc,
                    kSiteMmaKV);
-    OSATTN_STAMP(true, 2, j, 0);
+    OSATTN_STAMP(lead, 2, j, 0);
     if (ok && j == 0) {
-      if (n0 > 0) ok = mbar_wait(&bars->q_full[0], 0, wc, kSiteMmaQ);
-      if (ok && n1 > 0) ok = mbar_wait(&bars->q_full[1], 0, wc, kSiteMmaQ);
+      if (n0 > 0) ok = warp_wait(&bars->q_full[0], 0, wc, kSiteMmaQ);
+      if (ok && n1 > 0) ok = warp_wait(&bars->q_full[1], 0, wc, kSiteMmaQ);
     }
     if (!ok) break;
     tc_fence_after_sync();
     // tile 0: PV0(j-1), then S0(j)
     if (j > 0 && j - 1 < n0) {
-      ok = mbar_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
-      OSATTN_STAMP(true, 2, j, 1);
+      ok = warp_wait(&bars->p_full[0], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      OSATTN_STAMP(lead, 2, j, 1);
       if (!ok) break;
       tc_fence_after_sync();
-      mma_tmem_a_128<HD, kF16>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
-      if (j == n0) mma_commit(&bars->o_full[0]);
+      mma_tmem_a_128<HD, kF16, true>(o_col0, s_col0, v_desc + vs * kStageStep, j > 1);
+      if (j == n0) mma_commit<true>(&bars->o_full[0]);
     }
     if (j < n0) {
-      mma_abt_128<HD, kF16>(s_col0, q_desc0, k_desc + ks * kStageStep);
-      mma_commit(&bars->s_full[0]);
+      mma_abt_128<HD, kF16, true>(s_col0, q_desc0, k_desc + ks * kStageStep);
+      mma_commit<true>(&bars->s_full[0]);
     }
     // tile 1: PV1(j-1), then S1(j)
     if (j > 0 && j - 1 < n1) {
-      ok = mbar_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
-      OSATTN_STAMP(true, 2, j, 2);
+      ok = warp_wait(&bars->p_full[1], static_cast<uint32_t>(j - 1) & 1u, wc, kSiteMmaP);
+      OSATTN_STAMP(lead, 2, j, 2);
       if (!ok) break;
       tc_fence_after_sync();
-      mma_tmem_a_128<HD, kF16>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
-      if (j == n1) mma_commit(&bars->o_full[1]);
+      mma_tmem_a_128<HD, kF16, true>(o_col1, s_col1, v_desc + vs * kStageStep, j > 1);
+      if (j == n1) mma_commit<true>(&bars->o_full[1]);
     }
     if (j < n1) {
-      mma_abt_128<HD, kF16>(s_col1, q_desc1, k_desc + ks * kStageStep);
-      mma_commit(&bars->s_full[1]);
+      mma_abt_128<HD, kF16, true>(s_col1, q_desc1, k_desc + ks * kStageStep);
+      mma_commit<true>(&bars->s_full[1]);
     }
-    mma_commit(&bars->kv_empty[j % C::kIters]);
-    OSATTN_STAMP(true, 2, j, 3);
+    mma_commit<true>(&bars->kv_empty[j % C::kIters]);
+    OSATTN_STAMP(lead, 2, j, 3);
   }
-  // Every MMA this thread issued must complete before tensor memory is freed.
-  mma_commit(&bars->mma_drain);
+  // Every MMA the warp issued must complete before tensor memory is freed.
+  mma_commit<true>(&bars->mma_drain);
   drain_wait(&bars->mma_drain, 0, wc.limit_ns);
+  __syncwarp();
 }
 
 template <int HD, bool kSplit, bool kF16>
@@ -644,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<56>();
     if (warp == kProducerWarp && lane == 0 && n > 0)
       producer_role<HD>(&tmQ, &tmK, &tmV, bars, sQ, sKV, b, h, q0, n0, n1, sb, wc);
-    else if (warp == kMmaWarp && lane == 0 && n > 0)
+    else if (warp == kMmaWarp && n > 0)
       mma_role<HD, kF16>(bars, tmem, sQ, sKV, n0, n1, wc);
   }
 
