@@ -382,15 +382,16 @@ __device__ __forceinline__ void bwd_ds_part(uint32_t dp_addr, int c0, Dof4&& ndo
 // D (128 x N fp32) (+)= A B over 128 inner elements: A the 16-bit operand
 // the two warpgroups wrote (elements 0-63 in columns 0-31 of a_tmem,
 // 64-127 in 64-95), B an MN-major tile, 16 rows (2 KB) per MMA.
+// Issued warp-wide (one elected lane, see mma_ss_k).
 template <int N, bool kF16>
 __device__ __forceinline__ void mma_tmem_a_groups(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                   bool accumulate) {
   constexpr uint32_t id = idesc_f16_f32(128, N, 1, kF16);  // B is MN-major
-  mma_bf16_ts(d_tmem, a_tmem, b_desc, id, accumulate ? 1u : 0u);
+  mma_bf16_ts<true>(d_tmem, a_tmem, b_desc, id, accumulate ? 1u : 0u);
 #pragma unroll
   for (int kk = 1; kk < 8; ++kk)
-    mma_ts_k<1>(d_tmem, a_tmem + (kk / 4) * 64 + (kk % 4) * 8,
-                sdesc_add(b_desc, static_cast<uint32_t>((kk * 2048) >> 4)), id);
+    mma_ts_k<1, true>(d_tmem, a_tmem + (kk / 4) * 64 + (kk % 4) * 8,
+                      sdesc_add(b_desc, static_cast<uint32_t>((kk * 2048) >> 4)), id);
 }
 
 // ------------------------------------------------------------------ dK, dV
@@ -535,54 +536,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // S^T_{it+1}, dK += dS^T_it Q_it, dP^T_{it+1}.  The tensor core runs
     // them in issue order, so a product that overwrites a tile follows the
     // one that reads it.
-    if (lane == 0 && n_it > 0) {
+    if (n_it > 0) {  // the whole warp; one elected lane issues
       const uint64_t kA = sdesc_sw128(smem_u32(sK), 16, 1024);  // K-major A
       const uint64_t vA = sdesc_sw128(smem_u32(sV), 16, 1024);
-      bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
-      if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
+      bool ok = warp_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      if (ok) ok = warp_wait(&bars->full[0], 0, wc, kSiteBwdMma);
       if (ok) {
         tc_fence_after_sync();
         const uint32_t sq = smem_u32(ring), sdo = sq + C::kTileBytes;
-        mma_abt<128, HD, kF16>(tmem, kA, sdesc_sw128(sq, 16, 1024));
-        mma_commit(&bars->s_full[0]);
-        mma_abt<128, HD, kF16>(tmem + 128, vA, sdesc_sw128(sdo, 16, 1024));
-        mma_commit(&bars->dp_full);
+        mma_abt<128, HD, kF16, true>(tmem, kA, sdesc_sw128(sq, 16, 1024));
+        mma_commit<true>(&bars->s_full[0]);
+        mma_abt<128, HD, kF16, true>(tmem + 128, vA, sdesc_sw128(sdo, 16, 1024));
+        mma_commit<true>(&bars->dp_full);
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::kStages, s1 = (it + 1) % C::kStages;
         const uint32_t sq = smem_u32(ring + s * C::kStageBytes), sdo = sq + C::kTileBytes;
         const uint32_t nq = smem_u32(ring + s1 * C::kStageBytes), ndo = nq + C::kTileBytes;
         const bool more = it + 1 < n_it;
-        ok = mbar_wait(&bars->p_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        ok = warp_wait(&bars->p_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
         if (!ok) break;
         tc_fence_after_sync();
         // dV += P^T dO: B = dO read MN-major
         mma_tmem_a_groups<HD, kF16>(tmem + C::kColAcc0, tmem, sdesc_sw128(sdo, kT * 128, 1024), it > 0);
-        mma_commit(&bars->empty2[s]);
+        mma_commit<true>(&bars->empty2[s]);
         if (more) {
-          ok = mbar_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
+          ok = warp_wait(&bars->full[s1], static_cast<uint32_t>((it + 1) / C::kStages) & 1u, wc,
                          kSiteBwdMma);
           if (!ok) break;
           tc_fence_after_sync();
-          mma_abt<128, HD, kF16>(tmem, kA, sdesc_sw128(nq, 16, 1024));
-          mma_commit(&bars->s_full[0]);
+          mma_abt<128, HD, kF16, true>(tmem, kA, sdesc_sw128(nq, 16, 1024));
+          mma_commit<true>(&bars->s_full[0]);
         }
-        ok = mbar_wait(&bars->ds_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
+        ok = warp_wait(&bars->ds_full, static_cast<uint32_t>(it) & 1u, wc, kSiteBwdMma);
         if (!ok) break;
         tc_fence_after_sync();
         // dK += dS^T Q: B = Q read MN-major
         mma_tmem_a_groups<HD, kF16>(tmem + C::kColAcc1, tmem + 128, sdesc_sw128(sq, kT * 128, 1024),
                                     it > 0);
-        mma_commit(&bars->empty[s]);
+        mma_commit<true>(&bars->empty[s]);
         if (more) {
-          mma_abt<128, HD, kF16>(tmem + 128, vA, sdesc_sw128(ndo, 16, 1024));
-          mma_commit(&bars->dp_full);
+          mma_abt<128, HD, kF16, true>(tmem + 128, vA, sdesc_sw128(ndo, 16, 1024));
+          mma_commit<true>(&bars->dp_full);
         }
       }
-      if (ok) mma_commit(&bars->acc_full);
-      // Every MMA this thread issued must complete before tensor memory is freed.
-      mma_commit(&bars->mma_drain);
+      if (ok) mma_commit<true>(&bars->acc_full);
+      // Every MMA the warp issued must complete before tensor memory is freed.
+      mma_commit<true>(&bars->mma_drain);
       drain(&bars->mma_drain, 0, wc.limit_ns);
+      __syncwarp();
     }
   } else {
     // ---------------------------------------------------------------- elementwise
@@ -753,18 +755,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Order: S_0, dP_0; then per key tile j: S_{j+1} (other S buffer),
     // dQ += dS_j K_j, dP_{j+1}.  S_{j+1} overwrites S_{j-1}, whose reader
     // signalled ds_full for tile j - 1 before the previous dQ product.
-    if (lane == 0 && n_kt > 0) {
+    if (n_kt > 0) {  // the whole warp; one elected lane issues
       const uint64_t qA = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dA = sdesc_sw128(smem_u32(sdO), 16, 1024);
-      bool ok = mbar_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
-      if (ok) ok = mbar_wait(&bars->full[0], 0, wc, kSiteBwdMma);
+      bool ok = warp_wait(&bars->fixed_full, 0, wc, kSiteBwdMma);
+      if (ok) ok = warp_wait(&bars->full[0], 0, wc, kSiteBwdMma);
       if (ok) {
         tc_fence_after_sync();
-        mma_abt<128, HD, kF16>(tmem, qA, sdesc_sw128(smem_u32(kring), 16, 1024));
-        mma_commit(&bars->s_full[0]);
-        mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(smem_u32(vring), 16, 1024));
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->empty2[0]);
+        mma_abt<128, HD, kF16, true>(tmem, qA, sdesc_sw128(smem_u32(kring), 16, 1024));
+        mma_commit<true>(&bars->s_full[0]);
+        mma_abt<128, HD, kF16, true>(tmem + kDqColDP, dA, sdesc_sw128(smem_u32(vring), 16, 1024));
+        mma_commit<true>(&bars->dp_full);
+        mma_commit<true>(&bars->empty2[0]);
       }
       for (int j = 0; ok && j < n_kt; ++j) {
         const int a = j % C::kKSlots, a1 = (j + 1) % C::kKSlots, v1 = (j + 1) % C::kVSlots;
@@ -773,29 +775,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t nv = smem_u32(vring + v1 * C::kTileBytes);
         const bool more = j + 1 < n_kt;
         if (more) {
-          ok = mbar_wait(&bars->full[a1], static_cast<uint32_t>((j + 1) / C::kKSlots) & 1u, wc,
+          ok = warp_wait(&bars->full[a1], static_cast<uint32_t>((j + 1) / C::kKSlots) & 1u, wc,
                          kSiteBwdMma);
           if (!ok) break;
           tc_fence_after_sync();
-          mma_abt<128, HD, kF16>(tmem + 128 * ((j + 1) & 1), qA, sdesc_sw128(nk, 16, 1024));
-          mma_commit(&bars->s_full[(j + 1) & 1]);
+          mma_abt<128, HD, kF16, true>(tmem + 128 * ((j + 1) & 1), qA, sdesc_sw128(nk, 16, 1024));
+          mma_commit<true>(&bars->s_full[(j + 1) & 1]);
         }
-        ok = mbar_wait(&bars->ds_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
+        ok = warp_wait(&bars->ds_full, static_cast<uint32_t>(j) & 1u, wc, kSiteBwdMma);
         if (!ok) break;
         tc_fence_after_sync();
         // dQ += dS K: B = K_j read MN-major
         mma_tmem_a_groups<HD, kF16>(tmem + kDqColAcc, tmem + kDqColDP,
                                     sdesc_sw128(sk, kT * 128, 1024), j > 0);
-        mma_commit(&bars->empty[a]);
+        mma_commit<true>(&bars->empty[a]);
         if (more) {
-          mma_abt<128, HD, kF16>(tmem + kDqColDP, dA, sdesc_sw128(nv, 16, 1024));
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->empty2[v1]);
+          mma_abt<128, HD, kF16, true>(tmem + kDqColDP, dA, sdesc_sw128(nv, 16, 1024));
+          mma_commit<true>(&bars->dp_full);
+          mma_commit<true>(&bars->empty2[v1]);
         }
       }
-      if (ok) mma_commit(&bars->acc_full);
-      mma_commit(&bars->mma_drain);
+      if (ok) mma_commit<true>(&bars->acc_full);
+      mma_commit<true>(&bars->mma_drain);
       drain(&bars->mma_drain, 0, wc.limit_ns);
+      __syncwarp();
     }
   } else {
     const int c0 = 64 * (warp >> 2);  // this warpgroup's columns (keys) of each tile

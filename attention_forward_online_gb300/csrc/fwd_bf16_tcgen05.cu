@@ -491,12 +491,6 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 // control flow stays warp-uniform (a lane-0-only issuer let the tensor pipe
 // idle for about 150 cycles at each barrier wait).
 
-// A bounded wait whose result is the same in every lane of the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
-                                          uint32_t site) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, site));
-}
-
 template <int HD, bool kF16>
 __device__ __forceinline__ void mma_role(Bars* bars, uint32_t tmem, uint8_t* sQ, uint8_t* sKV,
                                          int n0, int n1, WaitCtl wc) {

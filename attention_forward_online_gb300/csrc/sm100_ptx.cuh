@@ -91,6 +91,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   return mbar_wait_slow(bar, parity, w, site);
 }
 
+// mbar_wait executed by a whole warp, with a result every lane agrees on
+// (and the warp converged again afterwards).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w,
+                                          uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
