@@ -635,7 +635,7 @@ def run_bwd(args, w):
             "max_abs_err": err,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "bwd_rowdot + bwd_dkdv + bwd_dq kernels, timed together",
+                         "kernel": "bwd_dq + bwd_dkdv kernels (D formed in the dQ kernel), timed together",
                          "peak_source": f"bf16_tflops (burst) of {peak_src}"},
             "cpu_baseline": {"value": round(cflops / secs / 1e12, 6), "unit": "TFLOPS",
                              "cores": cpu_cores(), "kind": "oracle",
