@@ -60,25 +60,30 @@ namespace osattn {
 
 // Profiling builds (OSATTN_STEP_TRACE=1, a separate library; never the
 // product) stamp the SM clock at each phase of every K/V step of the first
-// kTraceCtas CTAs: per softmax warpgroup t (role t) S seen / S in registers /
-// alpha published / P published, and in the MMA thread (role 2) K/V seen /
-// P_0 seen / P_1 seen / step issued.  osattn_step_trace_read copies them out.
+// kTraceCtas CTAs: per softmax warpgroup t (role t, its first warp) S seen /
+// S in registers / alpha published / P published; in the MMA warp (role 2)
+// K/V seen / P_0 seen / P_1 seen / step issued; P published by each of the
+// four softmax warps of tile t (role 3 + t, one stamp per warp); and per
+// correction of tile t (role 5 + t, its first warp) alpha seen / O rescaled
+// / arrived, with the fourth entry 1 if that warp rescaled O (not a clock).
+// osattn_step_trace_read copies them out.
 #ifndef OSATTN_STEP_TRACE
 #define OSATTN_STEP_TRACE 0
 #endif
-constexpr int kTraceCtas = 8, kTraceSteps = 128;
+constexpr int kTraceCtas = 8, kTraceRoles = 7, kTraceSteps = 128;
 #if OSATTN_STEP_TRACE
-__device__ long long g_step_trace[kTraceCtas][3][kTraceSteps][4];
-#define OSATTN_STAMP(cond, role, j, k)                                                  \
+__device__ long long g_step_trace[kTraceCtas][kTraceRoles][kTraceSteps][4];
+#define OSATTN_STAMP_VALUE(cond, role, j, k, value)                                     \
   do {                                                                                  \
     if ((cond) && blockIdx.x < kTraceCtas && (j) < kTraceSteps)                         \
-      g_step_trace[blockIdx.x][role][j][k] = clock64();                                 \
+      g_step_trace[blockIdx.x][role][j][k] = (value);                                   \
   } while (0)
 #else
-#define OSATTN_STAMP(cond, role, j, k) \
-  do {                                 \
+#define OSATTN_STAMP_VALUE(cond, role, j, k, value) \
+  do {                                              \
   } while (0)
 #endif
+#define OSATTN_STAMP(cond, role, j, k) OSATTN_STAMP_VALUE(cond, role, j, k, clock64())
 
 namespace {
 
@@ -296,6 +301,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     tc_fence_before_sync();
     mbar_arrive(&bars->p_full[t]);
     OSATTN_STAMP(row == 0, t, j, 3);
+    OSATTN_STAMP(lane == 0, 3 + t, j, quarter);
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -385,8 +391,11 @@ __device__ __forceinline__ void correction_tile(Bars* bars, uint32_t lane_base, 
   ok = mbar_wait(&bars->alpha_full[t], static_cast<uint32_t>(j) & 1u, wc, kSiteCorrAlpha);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return;
+  OSATTN_STAMP(row == 0, 5 + t, j, 0);
   const float alpha = bars->alpha[t][row];
-  if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+  const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+  OSATTN_STAMP_VALUE(row == 0, 5 + t, j, 3, rescale ? 1 : 0);
+  if (rescale) {
     tc_fence_after_sync();
     const uint64_t a2 = f2_pack(alpha, alpha);
     const uint32_t o_addr = lane_base + C::kOCol0 + static_cast<uint32_t>(t * HD);
@@ -408,8 +417,10 @@ __device__ __forceinline__ void correction_tile(Bars* bars, uint32_t lane_base, 
     }
     tmem_st_wait();
   }
+  OSATTN_STAMP(row == 0, 5 + t, j, 1);
   tc_fence_before_sync();
   mbar_arrive(&bars->p_full[t]);
+  OSATTN_STAMP(row == 0, 5 + t, j, 2);
 }
 
 template <int HD>
@@ -703,7 +714,7 @@ cudaError_t prepare_fwd_bf16() {
 }
 
 cudaError_t read_step_trace(void* host, size_t bytes, size_t* needed) {
-  *needed = static_cast<size_t>(kTraceCtas) * 3 * kTraceSteps * 4 * sizeof(long long);
+  *needed = static_cast<size_t>(kTraceCtas) * kTraceRoles * kTraceSteps * 4 * sizeof(long long);
 #if OSATTN_STEP_TRACE
   if (bytes < *needed) return cudaErrorInvalidValue;
   return cudaMemcpyFromSymbol(host, g_step_trace, *needed);

@@ -124,6 +124,18 @@ def print_step_trace(tr):
               f"S load {ld:.0f}, row max + alpha {mx:.0f}, P {pp:.0f} "
               f"(busy {ld + mx + pp:.0f}); P published -> next S seen (PV + S) {mma_lat:.0f}; "
               f"MMA issuer iteration {mma_iter:.0f}")
+        # P of tile 0 complete (last of the four softmax warps and the
+        # correction warp) -> seen by the MMA warp; warp spread of P
+        warps = tr[cta, 3][js]                       # [step, warp]
+        corr = tr[cta, 5][js]                        # alpha seen, rescaled, arrived, flag
+        last = np.maximum(warps.max(1), corr[:, 2])
+        seen = mma[js + 1, 1] - last
+        rel = (warps - warps[:, :1]).mean(0)
+        print(f"       tile 0: softmax warps publish P at {rel[1]:+.0f} / {rel[2]:+.0f} / "
+              f"{rel[3]:+.0f} cycles from its first warp; correction arrives "
+              f"{(corr[:, 2] - warps.max(1)).mean():+.0f} from the last of them and rescaled O "
+              f"in {100 * corr[:, 3].mean():.0f} % of steps; last arrival -> MMA warp sees P "
+              f"{seen.mean():.0f}")
 
 
 def run_rows(w, args):

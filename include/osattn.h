@@ -426,9 +426,13 @@ int osattn_last_timeout_site(void);
  * A library built with OSATTN_STEP_TRACE=1 (a separate profiling build,
  * never the product) records SM clock stamps at the phases of every K/V
  * step of the first 8 CTAs of each bf16/fp16 forward launch: long long
- * [8 CTAs][3 roles][128 steps][4 stamps]; role 0/1 = softmax of query tile
- * 0/1 (S seen, S in registers, alpha published, P published), role 2 = MMA
- * issuer (K/V seen, P of tile 0 seen, P of tile 1 seen, step issued).
+ * [8 CTAs][7 roles][128 steps][4 stamps]; role 0/1 = softmax of query tile
+ * 0/1, its first warp (S seen, S in registers, alpha published, P
+ * published); role 2 = MMA warp (K/V seen, P of tile 0 seen, P of tile 1
+ * seen, step issued); role 3/4 = P published by each of the four softmax
+ * warps of tile 0/1; role 5/6 = correction of tile 0/1, its first warp
+ * (alpha seen, O rescaled, arrived, and 1 if the warp rescaled O - a flag,
+ * not a clock).
  * Copies them to `host` (bytes >= *needed) after the stream has
  * synchronised.  *needed (if not NULL) gets the size.  Returns OSATTN_OK,
  * OSATTN_ERR_INVALID_ARG (buffer too small) or, in a product build,
