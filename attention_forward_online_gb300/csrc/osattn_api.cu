@@ -31,9 +31,10 @@ struct DeviceState {
   int row_cluster_max = 8;  // CTAs per cluster of the split-row softmax
   unsigned int* status = nullptr;  // device address of g_device_status
   // Offload pipeline (osattn_fwd_offload), created on first use: a
-  // host-to-device and a device-to-host copy stream and their events.
+  // host-to-device and a device-to-host copy stream, a second compute
+  // stream, and their events.
   bool offload_ready = false;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, cmp = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_final = nullptr;
   cudaEvent_t ev_in[kOffloadEvents] = {}, ev_out[kOffloadEvents] = {};
 };
@@ -269,6 +270,7 @@ int offload_streams(DeviceState* ds) {
   const unsigned ef = cudaEventDisableTiming;
   if (cudaStreamCreateWithFlags(&ds->h2d, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&ds->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&ds->cmp, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&ds->ev_entry, ef) != cudaSuccess ||
       cudaEventCreateWithFlags(&ds->ev_final, ef) != cudaSuccess)
     return OSATTN_ERR_CUDA;
@@ -290,18 +292,23 @@ struct OffloadSeg {
 
 // Host -> device -> host pipeline over chunks of heads: the copy of chunk
 // c + 1 in, the compute of chunk c and the copy of chunk c - 1 out run
-// concurrently on the library's two copy streams and the caller's stream.
-// compute(b, h0, nh) enqueues the work of heads h0 .. h0 + nh - 1 of batch
-// entry b on the caller's stream.
+// concurrently on the library's two copy streams and the compute streams.
+// With `alternate`, chunks alternate between the caller's stream and the
+// library's second compute stream, so that a chunk's launch can start on
+// the SMs the tail of the previous one leaves idle (for work whose chunks
+// touch disjoint parts of every buffer); otherwise all run on the caller's
+// stream.  compute(b, h0, nh, s) enqueues the work of heads
+// h0 .. h0 + nh - 1 of batch entry b on stream s.
 template <typename Compute>
 int offload_enqueue(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
-                    int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
+                    int n_in, const OffloadSeg* outs, int n_out, bool alternate, Compute&& compute) {
   int rc = OSATTN_OK;
   // Copies wait for the caller's earlier work on `stream` (it may still be
   // reading the device buffers).
   if (cudaEventRecord(ds->ev_entry, cs) != cudaSuccess ||
       cudaStreamWaitEvent(ds->h2d, ds->ev_entry, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(ds->d2h, ds->ev_entry, 0) != cudaSuccess)
+      cudaStreamWaitEvent(ds->d2h, ds->ev_entry, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(ds->cmp, ds->ev_entry, 0) != cudaSuccess)
     return OSATTN_ERR_CUDA;
   int c = 0;
   for (int b = 0; b < B; ++b) {
@@ -316,11 +323,12 @@ int offload_enqueue(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, cons
                             cudaMemcpyHostToDevice, ds->h2d) != cudaSuccess)
           return OSATTN_ERR_CUDA;
       }
-      if (cudaEventRecord(ein, ds->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, ein, 0) != cudaSuccess)
+      const cudaStream_t ks = (alternate && (c & 1)) ? ds->cmp : cs;
+      if (cudaEventRecord(ein, ds->h2d) != cudaSuccess || cudaStreamWaitEvent(ks, ein, 0) != cudaSuccess)
         return OSATTN_ERR_CUDA;
-      rc = compute(b, h0, nh);
+      rc = compute(b, h0, nh, ks);
       if (rc != OSATTN_OK) return rc;
-      if (cudaEventRecord(eout, cs) != cudaSuccess || cudaStreamWaitEvent(ds->d2h, eout, 0) != cudaSuccess)
+      if (cudaEventRecord(eout, ks) != cudaSuccess || cudaStreamWaitEvent(ds->d2h, eout, 0) != cudaSuccess)
         return OSATTN_ERR_CUDA;
       for (int i = 0; i < n_out; ++i) {
         const size_t off = head0 * outs[i].head_bytes;
@@ -338,16 +346,17 @@ int offload_enqueue(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, cons
 // shared), with both copy streams joined back into `stream` on every exit.
 template <typename Compute>
 int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, const OffloadSeg* ins,
-                     int n_in, const OffloadSeg* outs, int n_out, Compute&& compute) {
+                     int n_in, const OffloadSeg* outs, int n_out, bool alternate,
+                     Compute&& compute) {
   std::lock_guard<std::mutex> lock(g_offload_mutex);
   int rc = offload_streams(ds);
   if (rc != OSATTN_OK) return rc;
-  rc = offload_enqueue(ds, cs, B, H, hc, ins, n_in, outs, n_out, compute);
-  // `stream` completes only after the last copy, in either direction, even
-  // when the enqueue stopped part way (the caller may free the buffers once
-  // `stream` is done).
+  rc = offload_enqueue(ds, cs, B, H, hc, ins, n_in, outs, n_out, alternate, compute);
+  // `stream` completes only after the last copy, in either direction, and
+  // the last compute on the second stream, even when the enqueue stopped
+  // part way (the caller may free the buffers once `stream` is done).
   bool joined = true;
-  for (cudaStream_t cp : {ds->h2d, ds->d2h})
+  for (cudaStream_t cp : {ds->h2d, ds->d2h, ds->cmp})
     joined = joined && cudaEventRecord(ds->ev_final, cp) == cudaSuccess &&
              cudaStreamWaitEvent(cs, ds->ev_final, 0) == cudaSuccess;
   if (rc != OSATTN_OK) return rc;
@@ -355,12 +364,12 @@ int offload_pipeline(DeviceState* ds, cudaStream_t cs, int B, int H, int hc, con
 }
 
 // Heads per chunk: the caller's, or (0) enough that a chunk's launch covers
-// two waves of CTAs of `rows_per_cta` rows out of N.
-int offload_heads(int heads_per_chunk, int H, int N, int rows_per_cta, int num_sms) {
+// `waves` waves of CTAs of `rows_per_cta` rows out of N.
+int offload_heads(int heads_per_chunk, int H, int N, int rows_per_cta, int num_sms, int waves) {
   long long hc = heads_per_chunk;
   if (hc == 0) {
     const long long units = (N + rows_per_cta - 1) / rows_per_cta;
-    hc = (2LL * num_sms + units - 1) / units;
+    hc = (static_cast<long long>(waves) * num_sms + units - 1) / units;
   }
   return static_cast<int>(hc < H ? hc : H);
 }
@@ -376,8 +385,12 @@ int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, f
   DeviceState* ds = nullptr;
   rc = device_state(&ds);
   if (rc != OSATTN_OK) return rc;
-  // 256 query rows per CTA on the tensor cores, 16 in the fp32 kernel
-  const int hc = offload_heads(heads_per_chunk, H, Nq, dtype == OSATTN_FP32 ? 16 : 256, ds->num_sms);
+  // 256 query rows per CTA on the tensor cores, 16 in the fp32 kernel; one
+  // wave of CTAs a chunk (consecutive chunks overlap on two compute streams:
+  // on causal B1 H32 16K d128 from pinned host memory, 2.43 ms a call with
+  // 3-head chunks against 2.52 with 5)
+  const int hc = offload_heads(heads_per_chunk, H, Nq, dtype == OSATTN_FP32 ? 16 : 256, ds->num_sms,
+                               1);
   const size_t es = elem_size(dtype);
   const size_t qb = static_cast<size_t>(Nq) * d * es, kb = static_cast<size_t>(Nkv) * d * es;
   const size_t lb = static_cast<size_t>(Nq) * sizeof(float);
@@ -385,12 +398,13 @@ int fwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, f
                              {const_cast<void*>(Vh), Vd, kb}};
   const OffloadSeg outs[2] = {{Oh, Od, qb}, {LSEh, LSEd, lb}};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return offload_pipeline(ds, cs, B, H, hc, ins, 3, outs, 2, [&](int b, int h0, int nh) {
+  return offload_pipeline(ds, cs, B, H, hc, ins, 3, outs, 2, true, [&](int b, int h0, int nh,
+                                                                cudaStream_t ks) {
     const size_t head0 = static_cast<size_t>(b) * H + h0;
     return fwd_impl(static_cast<const char*>(Qd) + head0 * qb, static_cast<const char*>(Kd) + head0 * kb,
                     static_cast<const char*>(Vd) + head0 * kb, static_cast<char*>(Od) + head0 * qb,
                     LSEd + head0 * Nq, 1, nh, Nq, Nkv, d, nullptr, nullptr, nullptr, nullptr, scale,
-                    causal, key_len ? key_len + b : nullptr, dtype, cs);
+                    causal, key_len ? key_len + b : nullptr, dtype, ks);
   });
 }
 
@@ -418,7 +432,8 @@ int bwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, const void*
   rc = device_state(&ds);
   if (rc != OSATTN_OK) return rc;
   // 128 keys per dK/dV CTA on the tensor cores, 32 in the fp32 kernels
-  const int hc = offload_heads(heads_per_chunk, H, Nkv, dtype == OSATTN_FP32 ? 32 : 128, ds->num_sms);
+  const int hc = offload_heads(heads_per_chunk, H, Nkv, dtype == OSATTN_FP32 ? 32 : 128, ds->num_sms,
+                               2);
   const size_t es = elem_size(dtype);
   const size_t qb = static_cast<size_t>(Nq) * d * es, kb = static_cast<size_t>(Nkv) * d * es;
   const size_t lb = static_cast<size_t>(Nq) * sizeof(float);
@@ -427,7 +442,8 @@ int bwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, const void*
                              {const_cast<void*>(dOh), dOd, qb}, {const_cast<float*>(LSEh), LSEd, lb}};
   const OffloadSeg outs[3] = {{dQh, dQd, qb}, {dKh, dKd, kb}, {dVh, dVd, kb}};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return offload_pipeline(ds, cs, B, H, hc, ins, 6, outs, 3, [&](int b, int h0, int nh) {
+  return offload_pipeline(ds, cs, B, H, hc, ins, 6, outs, 3, false, [&](int b, int h0, int nh,
+                                                                cudaStream_t ks) {
     const size_t head0 = static_cast<size_t>(b) * H + h0;
     auto at = [&](const void* base, size_t head_bytes) {
       return static_cast<const char*>(base) + head0 * head_bytes;
@@ -435,11 +451,12 @@ int bwd_offload_impl(const void* Qh, const void* Kh, const void* Vh, const void*
     auto at_w = [&](void* base, size_t head_bytes) {
       return static_cast<char*>(base) + head0 * head_bytes;
     };
-    // The chunk's D goes at the start of the workspace: chunks run in order
-    // on `stream`, so the next chunk overwrites it only after its readers.
+    // The chunk's D goes at the start of the workspace: the chunks run in
+    // order on `stream` (this pipeline does not alternate compute streams),
+    // so the next chunk overwrites it only after its readers.
     return bwd_impl(at(Qd, qb), at(Kd, kb), at(Vd, kb), at(Od, qb), at(dOd, qb), LSEd + head0 * Nq,
                     at_w(dQd, qb), at_w(dKd, kb), at_w(dVd, kb), 1, nh, Nq, Nkv, d, nullptr, scale,
-                    causal, key_len ? key_len + b : nullptr, dtype, workspace, workspace_bytes, cs);
+                    causal, key_len ? key_len + b : nullptr, dtype, workspace, workspace_bytes, ks);
   });
 }
 
@@ -466,12 +483,12 @@ int softmax_rows_offload_impl(const void* in_h, void* out_h, float* lse_h, void*
   const OffloadSeg outs[2] = {{out_h, out, rb}, {lse_h, lse, sizeof(float)}};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return offload_pipeline(ds, cs, 1, static_cast<int>(rows), static_cast<int>(rc_rows), ins, 1, outs,
-                          lse ? 2 : 1, [&](int, int r0, int nr) {
+                          lse ? 2 : 1, true, [&](int, int r0, int nr, cudaStream_t ks) {
                             const size_t off = static_cast<size_t>(r0) * rb;
                             const cudaError_t e = osattn::launch_softmax_rows(
                                 static_cast<const char*>(in) + off, static_cast<char*>(out) + off,
                                 lse ? lse + r0 : nullptr, nr, N, dtype, ds->num_sms,
-                                ds->row_cluster_max, cs);
+                                ds->row_cluster_max, ks);
                             return e == cudaSuccess ? OSATTN_OK : OSATTN_ERR_CUDA;
                           });
 }

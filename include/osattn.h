@@ -132,7 +132,9 @@ int osattn_fwd_strided(const void* Q, const void* K, const void* V, void* O, flo
  * pipelined over chunks of heads so that the copy of one chunk in, the
  * attention of the previous one and the copy out of the one before that
  * overlap (one host-to-device and one device-to-host stream of the
- * library's, each chunk's attention on `stream`).  Same result as
+ * library's; the chunks' attention launches alternate between `stream` and
+ * a compute stream of the library's, so that one chunk's launch starts on
+ * the SMs the end of the previous one leaves idle).  Same result as
  * osattn_fwd on the copied data.
  *
  *   Q_host, K_host, V_host   host, contiguous [B, H, N, d] (read); pinned
@@ -144,7 +146,7 @@ int osattn_fwd_strided(const void* Q, const void* K, const void* V, void* O, flo
  *   B .. dtype               as for osattn_fwd (key_len is a device array)
  *   heads_per_chunk          heads per pipeline chunk, within one batch entry
  *                            (larger than H: one chunk per batch entry); 0
- *                            picks enough heads for two waves of CTAs per
+ *                            picks enough heads for one wave of CTAs per
  *                            chunk; negative -> OSATTN_ERR_INVALID_ARG
  *   stream                   the copies wait for work enqueued on `stream`
  *                            before the call, and `stream` completes only
@@ -291,8 +293,9 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
 /*
  * osattn_bwd_offload - osattn_bwd for tensors that live in host memory:
  * copies Q, K, V, O, dO and LSE in, computes the gradients and copies dQ,
- * dK and dV out, pipelined over chunks of heads exactly as
- * osattn_fwd_offload.  Same results as osattn_bwd on the copied data.
+ * dK and dV out, pipelined over chunks of heads as osattn_fwd_offload,
+ * except that every chunk's kernels run on `stream` (the chunks share the
+ * workspace's D).  Same results as osattn_bwd on the copied data.
  *
  *   *_host     host, contiguous (Q, O, dO, dQ [B, H, Nq, d]; K, V, dK, dV
  *              [B, H, Nkv, d]; LSE [B, H, Nq] fp32); inputs read, dQ_host,
