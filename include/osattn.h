@@ -293,9 +293,10 @@ int osattn_bwd(const void* Q, const void* K, const void* V, const void* O, const
 /*
  * osattn_bwd_offload - osattn_bwd for tensors that live in host memory:
  * copies Q, K, V, O, dO and LSE in, computes the gradients and copies dQ,
- * dK and dV out, pipelined over chunks of heads as osattn_fwd_offload,
- * except that every chunk's kernels run on `stream` (the chunks share the
- * workspace's D).  Same results as osattn_bwd on the copied data.
+ * dK and dV out, pipelined over chunks of heads as osattn_fwd_offload
+ * (when Nq is not a multiple of 4 every chunk's kernels run on `stream`:
+ * the chunks then share the start of the workspace).  Same results as
+ * osattn_bwd on the copied data.
  *
  *   *_host     host, contiguous (Q, O, dO, dQ [B, H, Nq, d]; K, V, dK, dV
  *              [B, H, Nkv, d]; LSE [B, H, Nq] fp32); inputs read, dQ_host,

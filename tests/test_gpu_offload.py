@@ -74,6 +74,8 @@ def test_offload_waits_for_earlier_work_on_the_stream():
     # B, H, Nq, Nkv, d, causal, key_len, heads_per_chunk
     (2, 5, 300, 300, 128, True, None, 2),
     (2, 3, 200, 333, 64, False, [333, 100], 0),
+    # Nq not a multiple of 4: the chunks run in order on one stream
+    (1, 4, 301, 256, 64, True, None, 1),
 ], ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[5] else "") + f"h{c[7]}")
 def test_bwd_offload_matches_device_call(case, dtype):
     B, H, Nq, Nkv, d, causal, kl, hpc = case
