@@ -66,13 +66,22 @@ namespace osattn {
 // four softmax warps of tile t (role 3 + t, one stamp per warp); and per
 // correction of tile t (role 5 + t, its first warp) alpha seen / O rescaled
 // / arrived, with the fourth entry 1 if that warp rescaled O (not a clock).
-// osattn_step_trace_read copies them out.
+// Every CTA below kTraceCtaTimes also records, in global-timer
+// nanoseconds, when it started, finished its setup, saw its first S, began
+// its epilogue (tile 0) and ended, and the SM it ran on.
+// osattn_step_trace_read copies both out.
 #ifndef OSATTN_STEP_TRACE
 #define OSATTN_STEP_TRACE 0
 #endif
-constexpr int kTraceCtas = 8, kTraceRoles = 7, kTraceSteps = 128;
+constexpr int kTraceCtas = 8, kTraceRoles = 7, kTraceSteps = 128, kTraceCtaTimes = 4096;
 #if OSATTN_STEP_TRACE
 __device__ long long g_step_trace[kTraceCtas][kTraceRoles][kTraceSteps][4];
+__device__ long long g_cta_times[kTraceCtaTimes][6];
+#define OSATTN_CTA_TIME(cond, k)                                                        \
+  do {                                                                                  \
+    if ((cond) && blockIdx.x < kTraceCtaTimes)                                          \
+      g_cta_times[blockIdx.x][k] = static_cast<long long>(global_timer_ns());           \
+  } while (0)
 #define OSATTN_STAMP_VALUE(cond, role, j, k, value)                                     \
   do {                                                                                  \
     if ((cond) && blockIdx.x < kTraceCtas && (j) < kTraceSteps)                         \
@@ -81,6 +90,9 @@ __device__ long long g_step_trace[kTraceCtas][kTraceRoles][kTraceSteps][4];
 #else
 #define OSATTN_STAMP_VALUE(cond, role, j, k, value) \
   do {                                              \
+  } while (0)
+#define OSATTN_CTA_TIME(cond, k) \
+  do {                           \
   } while (0)
 #endif
 #define OSATTN_STAMP(cond, role, j, k) OSATTN_STAMP_VALUE(cond, role, j, k, clock64())
@@ -237,6 +249,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     OSATTN_STAMP(row == 0, t, j, 0);
+    OSATTN_CTA_TIME(j == 0 && t == 0 && row == 0, 2);
     tc_fence_after_sync();
     uint32_t v[BN];
 #pragma unroll
@@ -305,6 +318,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
   }
 
   // ---------------------------------------------------------------- epilogue
+  OSATTN_CTA_TIME(t == 0 && row == 0, 3);
   if (ok && n_t > 0) {
     ok = mbar_wait(&bars->o_full[t], 0u, wc, kSiteEpiO);
     ok = __all_sync(0xffffffffu, ok);
@@ -571,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
   using C = Cfg<HD>;
   extern __shared__ uint8_t smem_raw[];
+  OSATTN_CTA_TIME(threadIdx.x == 0, 0);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
@@ -650,6 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort_flag, p.status, p.status + 1, p.wait_limit_ns};
+  OSATTN_CTA_TIME(threadIdx.x == 0, 1);
+#if OSATTN_STEP_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < kTraceCtaTimes) {
+    uint32_t sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    g_cta_times[blockIdx.x][5] = sm;
+  }
+#endif
 
   if (warp < kCorrWarp0) {
     regs_inc<184>();
@@ -671,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_st_wait();
   tc_fence_before_sync();
   __syncthreads();
+  OSATTN_CTA_TIME(threadIdx.x == 0, 4);
   if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after_sync();
@@ -714,10 +738,15 @@ cudaError_t prepare_fwd_bf16() {
 }
 
 cudaError_t read_step_trace(void* host, size_t bytes, size_t* needed) {
-  *needed = static_cast<size_t>(kTraceCtas) * kTraceRoles * kTraceSteps * 4 * sizeof(long long);
+  constexpr size_t kSteps = static_cast<size_t>(kTraceCtas) * kTraceRoles * kTraceSteps * 4;
+  constexpr size_t kCtas = static_cast<size_t>(kTraceCtaTimes) * 6;
+  *needed = (kSteps + kCtas) * sizeof(long long);
 #if OSATTN_STEP_TRACE
   if (bytes < *needed) return cudaErrorInvalidValue;
-  return cudaMemcpyFromSymbol(host, g_step_trace, *needed);
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_step_trace, kSteps * sizeof(long long));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyFromSymbol(static_cast<long long*>(host) + kSteps, g_cta_times,
+                              kCtas * sizeof(long long));
 #else
   (void)host;
   (void)bytes;

@@ -114,8 +114,9 @@ def lib():
 
 
 def step_trace():
-    """The per-step clock stamps of a profiling build (OSATTN_STEP_TRACE=1;
-    see include/osattn.h) as a numpy int64 array [8, 7, 128, 4]."""
+    """The clock stamps of a profiling build (OSATTN_STEP_TRACE=1; see
+    include/osattn.h): (per-step stamps, a numpy int64 array [8, 7, 128, 4];
+    per-CTA times, [4096, 6])."""
     import numpy as np
 
     need = ctypes.c_size_t(0)
@@ -124,7 +125,8 @@ def step_trace():
     st = lib().osattn_step_trace_read(buf.ctypes.data, buf.nbytes, ctypes.byref(need))
     if st != OK:
         raise OsattnError(st, "osattn_step_trace_read")
-    return buf.reshape(8, 7, 128, 4)
+    n = 8 * 7 * 128 * 4
+    return buf[:n].reshape(8, 7, 128, 4), buf[n:].reshape(4096, 6)
 
 
 def status_string(status: int) -> str:

@@ -97,7 +97,9 @@ def main(argv=None):
           f"{flops / (med * 1e-3) / 1e12:.1f} TFLOPS (first launch excluded); "
           f"ms {['%.4f' % m for m in ms]}")
     if args.step_trace:
-        print_step_trace(osattn.step_trace())
+        steps, ctas = osattn.step_trace()
+        print_step_trace(steps)
+        print_cta_times(ctas, grid_ctas(w))
     return 0
 
 
@@ -136,6 +138,39 @@ def print_step_trace(tr):
               f"{(corr[:, 2] - warps.max(1)).mean():+.0f} from the last of them and rescaled O "
               f"in {100 * corr[:, 3].mean():.0f} % of steps; last arrival -> MMA warp sees P "
               f"{seen.mean():.0f}")
+
+
+def grid_ctas(w):
+    """CTAs of one bf16/fp16 forward launch: 256 query rows each (times the
+    key ranges with split-KV)."""
+    return w.B * w.H * ((w.Nq + 255) // 256) * max(1, getattr(w, "splits", 0) or 1)
+
+
+def print_cta_times(ct, n):
+    """Where each CTA's time goes (the profiling build's per-CTA global-timer
+    stamps: start, setup done, first S seen, epilogue start, end, SM), over
+    the first min(n, 4096) CTAs of the last launch, and how busy the SMs were
+    between the first start and the last end."""
+    import numpy as np
+
+    ct = ct[:min(n, ct.shape[0])].astype(np.float64)
+    ok = ct[:, 4] > 0
+    ct = ct[ok]
+    if len(ct) == 0:
+        return
+    start, setup, s0, epi, end, sm = (ct[:, i] for i in range(6))
+    t0, t1 = start.min(), end.max()
+    busy = sum((end[sm == s] - start[sm == s]).sum() for s in np.unique(sm))
+    gaps = []
+    for s in np.unique(sm):
+        o = np.argsort(start[sm == s])
+        st, en = start[sm == s][o], end[sm == s][o]
+        gaps += list(st[1:] - en[:-1])
+    med = lambda x: float(np.median(x)) / 1e3
+    print(f"CTAs {len(ct)} on {len(np.unique(sm))} SMs over {(t1 - t0) / 1e3:.1f} us; per CTA "
+          f"(median, us): setup {med(setup - start):.2f}, to the first S {med(s0 - setup):.2f}, "
+          f"K/V loop {med(epi - s0):.2f}, epilogue {med(end - epi):.2f}; gap between CTAs on an "
+          f"SM {med(gaps) if gaps else 0.0:.2f}; SMs busy {busy / (len(np.unique(sm)) * (t1 - t0)):.3f}")
 
 
 def run_rows(w, args):

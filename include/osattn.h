@@ -436,7 +436,9 @@ int osattn_last_timeout_site(void);
  * seen, step issued); role 3/4 = P published by each of the four softmax
  * warps of tile 0/1; role 5/6 = correction of tile 0/1, its first warp
  * (alpha seen, O rescaled, arrived, and 1 if the warp rescaled O - a flag,
- * not a clock).
+ * not a clock).  Then long long [4096 CTAs][6] for the first 4096 CTAs of
+ * the last launch: global-timer nanoseconds at start, end of setup, first S
+ * seen, epilogue start (tile 0) and end, and the SM it ran on.
  * Copies them to `host` (bytes >= *needed) after the stream has
  * synchronised.  *needed (if not NULL) gets the size.  Returns OSATTN_OK,
  * OSATTN_ERR_INVALID_ARG (buffer too small) or, in a product build,

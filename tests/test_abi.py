@@ -354,4 +354,4 @@ def test_step_trace_hook_is_unsupported_in_the_product_build(L):
     need = ctypes.c_size_t(0)
     rc = L.osattn_step_trace_read(None, 0, ctypes.byref(need))
     assert rc == osattn.ERR_UNSUPPORTED
-    assert need.value == 8 * 7 * 128 * 4 * 8
+    assert need.value == (8 * 7 * 128 * 4 + 4096 * 6) * 8

@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 @pytest.mark.gpu
 def test_step_trace_stamps_follow_the_kernel_phases():
     from attention_forward_online_gb300 import _build, osattn
-    from attention_forward_online_gb300.run_workload import print_step_trace
+    from attention_forward_online_gb300.run_workload import print_cta_times, print_step_trace
 
     L = ctypes.CDLL(_build.build(step_trace=True))
     vp, i32 = ctypes.c_void_p, ctypes.c_int
@@ -36,10 +36,11 @@ def test_step_trace_stamps_follow_the_kernel_phases():
     torch.cuda.synchronize()
     need = ctypes.c_size_t(0)
     L.osattn_step_trace_read(None, 0, ctypes.byref(need))
-    assert need.value == 8 * 7 * 128 * 4 * 8
+    assert need.value == (8 * 7 * 128 * 4 + 4096 * 6) * 8
     buf = np.zeros(need.value // 8, dtype=np.int64)
     assert L.osattn_step_trace_read(buf.ctypes.data, buf.nbytes, ctypes.byref(need)) == osattn.OK
-    tr = buf.reshape(8, 7, 128, 4)
+    tr = buf[:8 * 7 * 128 * 4].reshape(8, 7, 128, 4)
+    ct = buf[8 * 7 * 128 * 4:].reshape(4096, 6)
     # the first CTAs run the longest causal units, one per head: CTAs 0-3 the
     # last 256 rows of heads 0-3 (31 and 32 K/V steps for tiles 0 and 1),
     # CTAs 4-7 the 256 rows before them (29 and 30)
@@ -58,3 +59,10 @@ def test_step_trace_stamps_follow_the_kernel_phases():
         assert set(np.unique(corr[:, 3])) <= {0, 1}
         assert corr[0, 3] == 0                               # no O to rescale at the first step
     print_step_trace(tr[:2])
+    # per-CTA times: the launch's 64 CTAs (4 heads x 16 query blocks), each
+    # start <= setup done <= first S <= epilogue <= end, on a valid SM
+    n = 4 * 16
+    c = ct[:n]
+    assert (np.diff(c[:, :5], axis=1) >= 0).all(), c[:4]
+    assert ((c[:, 5] >= 0) & (c[:, 5] < 1024)).all()
+    print_cta_times(ct, n)
