@@ -201,7 +201,8 @@ __device__ __forceinline__ int tile_kv_count(int q0, int Nq, int kv_len, int cau
   return (kv_end + BN - 1) / BN;
 }
 
-// Row max / min over 128 values: 3-input instructions in 8 chains.
+// Row max over 128 values (tiles crossing the mask): 3-input instructions in
+// 8 chains.
 __device__ __forceinline__ float max128(const uint32_t* v) {
   float a[8];
 #pragma unroll
@@ -212,18 +213,6 @@ __device__ __forceinline__ float max128(const uint32_t* v) {
     for (int i = 0; i < 8; ++i)
       a[i] = fmax3(a[i], __uint_as_float(v[j + i]), __uint_as_float(v[j + 8 + i]));
   return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-}
-
-__device__ __forceinline__ float min128(const uint32_t* v) {
-  float a[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = fminf(__uint_as_float(v[i]), __uint_as_float(v[i + 8]));
-#pragma unroll
-  for (int j = 16; j < BN; j += 16)
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      a[i] = fmin3(a[i], __uint_as_float(v[j + i]), __uint_as_float(v[j + 8 + i]));
-  return fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fminf(a[6], a[7]));
 }
 
 // ------------------------------------------------------------------ softmax
@@ -251,12 +240,26 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
     OSATTN_STAMP(row == 0, t, j, 0);
     OSATTN_CTA_TIME(j == 0 && t == 0 && row == 0, 2);
     tc_fence_after_sync();
+    // S in registers, with the max (scale >= 0) or min (scale < 0) of each
+    // 32-column chunk formed by the loads: an unmasked tile's row max needs
+    // no pass over the 128 values.
     uint32_t v[BN];
+    float ext[BN / 32];
+    if (c >= 0.f) {
 #pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) tmem_ld_32x32b_x32(s_addr + ch * 32, v + ch * 32);
+      for (int ch = 0; ch < BN / 32; ++ch)
+        tmem_ld_red_32x32b_x32<true>(s_addr + ch * 32, v + ch * 32, ext[ch]);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < BN / 32; ++ch)
+        tmem_ld_red_32x32b_x32<false>(s_addr + ch * 32, v + ch * 32, ext[ch]);
+    }
     tmem_ld_wait();
 #pragma unroll
-    for (int ch = 0; ch < BN / 32; ++ch) reg_fence32(v + ch * 32);
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      reg_fence32(v + ch * 32);
+      asm volatile("" : "+f"(ext[ch]));
+    }
     OSATTN_STAMP(row == 0, t, j, 1);
 
     // x_j = s_j * c (log2 units).  Unmasked tiles keep raw s in v and fold
@@ -272,7 +275,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, Bars* bars, uint32
       cm = 1.f;
       m_new = fmaxf(m, max128(v));
     } else {
-      m_new = fmaxf(m, (c >= 0.f ? max128(v) : min128(v)) * c);
+      // max_j(s_j * c) = c * max_j s_j for c >= 0, c * min_j s_j otherwise
+      static_assert(BN == 128, "four 32-column chunks");
+      const float e4 = c >= 0.f ? fmaxf(fmaxf(ext[0], ext[1]), fmaxf(ext[2], ext[3]))
+                                : fminf(fminf(ext[0], ext[1]), fminf(ext[2], ext[3]));
+      m_new = fmaxf(m, e4 * c);
     }
     const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_new);
     bars->alpha[t][row] = alpha;

@@ -193,6 +193,32 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
       : "r"(taddr));
 }
 
+// tcgen05.ld with a min / max reduction (sm_103a): the same 32 lanes x 32
+// columns into r[0..31] as tmem_ld_32x32b_x32, and in red the max (kMax) or
+// min of the 32 values this thread receives, formed by the load.  red is
+// valid only after tmem_ld_wait(), like r.  (tests/probes/tmem_ld_red.cu
+// checks both against the stored values.)
+template <bool kMax>
+__device__ __forceinline__ void tmem_ld_red_32x32b_x32(uint32_t taddr, uint32_t* r, float& red) {
+#define OSATTN_LD_RED(OP)                                                                   \
+  asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32." OP ".f32 "                          \
+               "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "     \
+               "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, " \
+               "%32, [%33];"                                                                  \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),      \
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),    \
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),             \
+                 "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),             \
+                 "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),             \
+                 "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(red)   \
+               : "r"(taddr))
+  if constexpr (kMax)
+    OSATTN_LD_RED("max");
+  else
+    OSATTN_LD_RED("min");
+#undef OSATTN_LD_RED
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
