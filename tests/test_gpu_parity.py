@@ -71,6 +71,41 @@ def test_edge_shapes_full_parity(case, dtype):
     check(O, L, Oref, Lref, kind_of(q))
 
 
+SCALES = [
+    # B, H, Nq, Nkv, d, causal, key_len, scale
+    (1, 2, 300, 700, 128, False, None, -1 / math.sqrt(128)),
+    (2, 1, 384, 384, 64, True, [384, 200], -1 / math.sqrt(64)),
+    (1, 1, 257, 513, 128, True, None, -2.0),
+    (1, 2, 200, 333, 64, False, [333], 0.0),
+    (1, 1, 300, 300, 128, True, None, 0.0),
+    (1, 1, 256, 640, 64, False, None, 2.0),
+]
+
+
+# fp32 runs the cases with |scale| <= 1/sqrt(d) only: its 1e-5 gate is the
+# stated fp32 tolerance for logits of std up to 8, and a scale of 2 at d = 128
+# gives logits of std ~23, where rounding one 128-term fp32 dot product alone
+# moves the LSE by ~1e-5.
+SCALE_RUNS = [(c, dt) for c in SCALES for dt in KIND
+              if dt is not torch.float32 or abs(c[7]) <= 1 / math.sqrt(c[4])]
+
+
+@pytest.mark.parametrize(
+    "case,dtype", SCALE_RUNS,
+    ids=["x".join(map(str, c[:5])) + ("c" if c[5] else "") + f"s{c[7]:.3g}-{KIND[dt]}"
+         for c, dt in SCALE_RUNS])
+def test_negative_zero_and_large_scale_full_parity(case, dtype):
+    """The scale enters the softmax as s * scale: for a negative scale the
+    row max of s * scale is scale times the row MIN of s, which the bf16/fp16
+    kernel takes from its tensor-memory loads (the min reduction) on unmasked
+    tiles; zero gives uniform weights.  Every output against the oracle."""
+    B, H, Nq, Nkv, d, causal, kl, scale = case
+    q, k, v = make_qkv(B, H, Nq, Nkv, d, dtype, seed=2000 + Nq + Nkv, q_std=1.0)
+    O, L = run_gpu(q, k, v, scale, causal, kl)
+    Oref, Lref = oracle.attention_fwd(q, k, v, scale, causal, kl)
+    check(O, L, Oref, Lref, kind_of(q))
+
+
 @pytest.mark.parametrize("dtype", list(KIND), ids=list(KIND.values()))
 def test_worked_example_through_kernel(dtype):
     # Logits (1, 5, 3) for one query (chapter 6 §6.3.2), V = identity on the
