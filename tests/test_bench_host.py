@@ -147,3 +147,21 @@ def test_other_configs_default_only_with_the_default_workload(monkeypatch):
     seen.clear()
     bench.main(["--steps", "3", "--no-other-configs"])
     assert seen["args"].other_configs is False
+
+
+def test_forward_profiles_name_the_current_kernel_source():
+    # Every committed summary of the forward kernel (the three workloads, the
+    # bench's launch list and the split-KV workload) names the kernel source
+    # hash bench.py reports, so a kernel change cannot leave them silently
+    # describing another build.
+    import glob
+    import os
+
+    sha = bench.kernel_source_hash()
+    paths = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "fwd_bf16_kernel__*.md")))
+    paths += [os.path.join(bench.ROOT, "profiles", "launches__bench_default.md"),
+              os.path.join(bench.ROOT, "profiles", "splitkv__bf16_b1_h8_q512_kv65536_d128.md")]
+    assert len(paths) == 5
+    for p in paths:
+        with open(p) as f:
+            assert f"`{sha}`" in f.read(), os.path.basename(p)
